@@ -67,6 +67,7 @@ def test_gemm_brute_force_tiny(oracle_mod):
             # dequantize rounds code*s*g once to fp32: relative 2^-24 per term
             assert abs(d[m, n] - s) <= 2 ** -23 * t + 1e-300
             assert abs(bound[m, n] - t) <= 2 ** -23 * t
-    # the rows= subset equals the corresponding rows of the full product
-    d2, _ = oracle_mod.gemm_reference(qa, qb, rows=np.array([4, 1]))
-    assert (d2 == d[[4, 1]]).all()
+    # the rows= subset equals the corresponding rows of the full product (up to
+    # the fp64 summation order of the matmul)
+    d2, b2 = oracle_mod.gemm_reference(qa, qb, rows=np.array([4, 1]))
+    assert (np.abs(d2 - d[[4, 1]]) <= 1e-14 * b2).all()
