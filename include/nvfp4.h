@@ -1,0 +1,183 @@
+/*
+ * nvfp4.h - C ABI of the B300 (sm_103a) NVFP4 quantizer and block-scaled GEMM.
+ *
+ * The format ("NVIDIA Introduces a 4-Bit Pretraining Methodology Using NVFP4",
+ * section "Summary"): 16-element blocks of 4-bit E2M1 codes, one E4M3 scale per
+ * block and one FP32 scale per tensor.  The recipe components ("Method" on the
+ * same page; the hyper.ai story "NVIDIA présente NVFP4"): 2D 16x16 weight
+ * blocks, a 16x16 Random Hadamard Transform on Wgrad inputs, stochastic
+ * rounding on gradients.  Four-over-Six per-block scaling: the hyper.ai story
+ * on the Nemotron 3 Ultra NVFP4 checkpoint.
+ *
+ * Arithmetic of the encoder (fl = one IEEE fp32 op, round to nearest even):
+ *   amax = max |x| over the tensor (after the RHT when it is on)
+ *   g    = fl(amax / 2688)   (2688 = 6 * 448; g = 1 when amax = 0)
+ *   per block:  amax_b = max |x| over the block
+ *               s_b = E4M3_rne_satfinite(fl(amax_b / fl(m * g))), m = 6
+ *                     (Four-over-Six: also m = 4, keep the candidate whose
+ *                      block squared error is strictly lower)
+ *               S_b = fl(s_b * g);  r_b = S_b == 0 ? 0 : fl(1 / S_b)
+ *   per element: code = E2M1(fl(x * r_b)), round to nearest even or stochastic,
+ *               saturating at +-6, sign bit copied from the product
+ *   decode:     y = fl(fl(value(code) * s_b) * g)
+ *
+ * Memory conventions (all functions):
+ *  - Every pointer named "device" is CUDA device memory owned by the caller.
+ *    The library never allocates device memory and never synchronises, except
+ *    nvfp4_sync_check.  `stream` is a cudaStream_t (NULL = legacy default).
+ *  - Arguments are validated on the host before any launch; a non-OK status
+ *    means nothing was launched.  Asynchronous faults surface at the next CUDA
+ *    call or in nvfp4_sync_check.
+ *  - Supported range: finite inputs whose tensor amax is 0 or at least 2^-90
+ *    (below that the block reciprocal may overflow).
+ */
+#ifndef NVFP4_H_
+#define NVFP4_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  NVFP4_OK = 0,
+  NVFP4_ERR_INVALID_ARG = 1,       /* null pointer, bad enum, negative size */
+  NVFP4_ERR_UNSUPPORTED_SHAPE = 2, /* shape rule broken (see each function) */
+  NVFP4_ERR_MISALIGNED = 3,        /* pointer or leading dimension not 16-byte aligned */
+  NVFP4_ERR_CUDA = 4,              /* a CUDA runtime/driver call failed */
+  NVFP4_ERR_TIMEOUT = 5            /* a GEMM pipeline wait ran out (reported by nvfp4_sync_check) */
+} nvfp4_status;
+
+typedef enum { NVFP4_F32 = 0, NVFP4_BF16 = 1 } nvfp4_dtype;
+typedef enum { NVFP4_BLOCK_1D = 0 /* 1 x 16 along K */, NVFP4_BLOCK_2D = 1 /* 16 x 16 */ } nvfp4_block;
+typedef enum { NVFP4_ROUND_RNE = 0, NVFP4_ROUND_STOCHASTIC = 1 } nvfp4_round;
+typedef enum { NVFP4_SCALE_MAX6 = 0, NVFP4_SCALE_FOUR_OVER_SIX = 1 } nvfp4_scaling;
+
+/* A quantized tensor in its K-major orientation: `rows` x `cols`, K = cols.
+ *   codes  device uint8 [rows][cols/2]; element 2j in the low nibble of byte j,
+ *          2j+1 in the high nibble.  E2M1 code: bit 3 sign, bits 0-2 index
+ *          into {0, 0.5, 1, 1.5, 2, 3, 4, 6}.
+ *   scales device uint8, nvfp4_scales_bytes(rows, cols) bytes: the E4M3 block
+ *          scales in the tensor-core scale tile layout.  The logical matrix
+ *          [rows][cols/16] is cut into 128-row x 4-column atoms of 512 bytes;
+ *          atom (r/128, kb/4) starts at ((r/128) * ceil(cols/64) + kb/4) * 512
+ *          and holds entry (r, kb) at (r%32)*16 + ((r%128)/32)*4 + kb%4.
+ *          Padding entries are written as 0 by the quantizer.
+ *   global_scale device float[1]: g.
+ *   amax   device float[1]: the tensor amax the encoder used. */
+typedef struct {
+  uint8_t* codes;
+  uint8_t* scales;
+  float* global_scale;
+  float* amax;
+  int64_t rows;
+  int64_t cols;
+} nvfp4_tensor;
+
+/* Options of one quantize call.
+ *   block      1D (activations, gradients) or 2D 16x16 (weights; W and W^T get
+ *              the same codes, so a 2D-quantized weight serves both GEMMs).
+ *   round      RNE, or stochastic from a Philox4x32-10 stream (gradients).
+ *   scaling    max-6 or Four-over-Six.
+ *   transpose  0: quantize x (K = cols of x); 1: quantize x^T (K = rows of x,
+ *              the output has cols(x) rows) - the layout Wgrad operands need.
+ *   seed, offset  the stochastic-rounding stream: element (r, k) of the output
+ *              orientation, i = r*K + k, draws 16 bits: half (i & 1) (high for
+ *              odd i) of word (i%8)/2 of Philox4x32-10(key = seed,
+ *              counter = (i/8 low, i/8 high, offset low, offset high)); the
+ *              element rounds up iff u16 < fl(frac * 65536). */
+typedef struct {
+  nvfp4_block block;
+  nvfp4_round round;
+  nvfp4_scaling scaling;
+  int transpose;
+  uint64_t seed;
+  uint64_t offset;
+} nvfp4_quant_config;
+
+/* Byte sizes of the buffers of a rows x cols (K = cols) quantized tensor. */
+size_t nvfp4_codes_bytes(int64_t rows, int64_t cols);
+size_t nvfp4_scales_bytes(int64_t rows, int64_t cols); /* ceil(rows/128)*128 * ceil(cols/64)*4 */
+
+/*
+ * nvfp4_quantize - BF16/FP32 tensor -> NVFP4 (codes, block scales, g, amax).
+ *   x        device, row-major [rows][ld] of dtype xt (only the first `cols`
+ *            columns are read).  16-byte aligned; ld * sizeof(xt) % 16 == 0.
+ *   cfg      host pointer, read during the call only.
+ *   amax_in  device float[1] or NULL.  NULL: the library first reduces max|x|
+ *            (one extra read of x).  Given: used as the tensor amax and copied
+ *            to out->amax.
+ *   out      host struct with device buffers sized for the OUTPUT orientation:
+ *            out->rows = transpose ? cols : rows, out->cols = transpose ? rows : cols.
+ * Shape rules: K (= out->cols) % 16 == 0; transpose = 1 needs cols % 16 == 0;
+ * 2D blocks need out->rows % 16 == 0.  Empty tensors (rows or cols 0) return OK.
+ */
+nvfp4_status nvfp4_quantize(const void* x, nvfp4_dtype xt, int64_t rows, int64_t cols, int64_t ld,
+                            const nvfp4_quant_config* cfg, const float* amax_in, nvfp4_tensor* out,
+                            void* stream);
+
+/*
+ * nvfp4_rht_quantize - the Wgrad operand path: 16x16 Random Hadamard Transform
+ * along the contraction dimension, then quantization (1D blocks).
+ *   Every 16-chunk of K of the output orientation is replaced by
+ *   y = 1/4 * H16 * diag(sigma) * x, H16 the Sylvester Hadamard matrix
+ *   (H[i][j] = (-1)^popcount(i&j)), sigma_i = -1 iff bit i of word 0 of
+ *   Philox4x32-10(key = rht_seed, counter = (0, 0x80000000, 0, 0)).  One sign
+ *   vector per seed: pass the same rht_seed for dY and X so that the transform
+ *   cancels in dY^T X.  The amax and the scales are those of the transformed
+ *   values.  cfg->block must be 1D; cfg->transpose selects K as for
+ *   nvfp4_quantize (Wgrad operands use transpose = 1, K = tokens).
+ *   transformed_debug  device fp32 [out->rows][out->cols] or NULL: receives
+ *            the transformed values that were encoded (for tests).
+ */
+nvfp4_status nvfp4_rht_quantize(const void* x, nvfp4_dtype xt, int64_t rows, int64_t cols, int64_t ld,
+                                const nvfp4_quant_config* cfg, uint64_t rht_seed, const float* amax_in,
+                                nvfp4_tensor* out, float* transformed_debug, void* stream);
+
+/*
+ * nvfp4_dequantize - y = fl(fl(value(code) * s_b) * g), BF16 output rounded
+ * from that fp32 value (nearest even).
+ *   q  host struct with device buffers (codes, scales, global_scale read).
+ *   y  device, row-major [q->rows][q->cols] of dtype yt, 16-byte aligned.
+ */
+nvfp4_status nvfp4_dequantize(const nvfp4_tensor* q, void* y, nvfp4_dtype yt, void* stream);
+
+/*
+ * nvfp4_gemm - D = g_A * g_B * sum_k (a_mk * s^A_{m,k/16}) * (b_nk * s^B_{n,k/16})
+ * on the tensor cores (block-scaled FP4 x FP4, FP32 accumulation), W4A4 as the
+ * Nemotron 3 Ultra story says Blackwell runs natively.
+ *   A  M x K NVFP4 (A->rows = M, A->cols = K), B  N x K NVFP4: both K-major.
+ *   D  device row-major [M][ldd] of dtype dt (FP32 or BF16 rounded to nearest
+ *      even from the fp32 result); ldd >= N, ldd * sizeof(dt) % 16 == 0.
+ * Shape rules: K % 256 == 0, M % 128 == 0, N % 128 == 0 (every workload of the
+ * recipe meets them); codes and scales 16-byte aligned.
+ */
+nvfp4_status nvfp4_gemm(const nvfp4_tensor* A, const nvfp4_tensor* B, void* D, nvfp4_dtype dt, int64_t ldd,
+                        void* stream);
+
+/*
+ * nvfp4_gemm_grouped - `count` independent GEMMs D[e] = A[e] * B[e]^T in one
+ * launch (routed experts).  A, B: host arrays of `count` tensors; D: host
+ * array of `count` device pointers, each row-major [M_e][N_e] (ldd = N_e).
+ * Every group follows the nvfp4_gemm shape rules; count <= NVFP4_MAX_GROUPS.
+ */
+#define NVFP4_MAX_GROUPS 128
+nvfp4_status nvfp4_gemm_grouped(int count, const nvfp4_tensor* A, const nvfp4_tensor* B, void* const* D,
+                                nvfp4_dtype dt, void* stream);
+
+/* Synchronise `stream`, then report (and clear) a pending CUDA error or a
+ * GEMM pipeline timeout recorded on the device. */
+nvfp4_status nvfp4_sync_check(void* stream);
+
+/* Human-readable status name (static string). */
+const char* nvfp4_status_string(nvfp4_status s);
+
+/* Text of the last error this thread's calls produced (static per thread). */
+const char* nvfp4_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* NVFP4_H_ */

@@ -1,0 +1,197 @@
+// Device helpers of the NVFP4 kernels (sm_103a).  Every fp32 operation that
+// decides a code or a scale is an explicit IEEE round-to-nearest intrinsic
+// (__fmul_rn, __fdiv_rn, __frcp_rn, __fadd_rn, __fsub_rn) so that the
+// compiler cannot contract or reorder it; the encoder's results are therefore
+// fixed bit for bit by the sequence written in nvfp4.h.
+#pragma once
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace nvfp4 {
+
+// --------------------------------------------------------------------------
+// Element formats
+// --------------------------------------------------------------------------
+
+// Eight fp32 values -> eight E2M1 codes, round to nearest even, saturating at
+// +-6.  Byte j of the result holds code(x[2j]) in its low nibble and
+// code(x[2j+1]) in its high nibble (the cvt puts its first operand high).
+__device__ __forceinline__ uint32_t e2m1x8_rne(const float* x) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(r)
+      : "f"(x[0]), "f"(x[1]), "f"(x[2]), "f"(x[3]), "f"(x[4]), "f"(x[5]), "f"(x[6]), "f"(x[7]));
+  return r;
+}
+
+// fp32 (>= 0) -> E4M3 byte, round to nearest even, saturating at 448.
+__device__ __forceinline__ uint32_t e4m3_rne_sat(float t) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(t));
+  return r & 0xFFu;
+}
+
+// E4M3 byte (sign clear, not NaN) -> fp32, exact.
+__device__ __forceinline__ float e4m3_value(uint32_t b) {
+  uint32_t e = (b >> 3) & 15u, m = b & 7u;
+  return e ? __uint_as_float(((e + 120u) << 23) | (m << 20)) : __fmul_rn((float)m, 0.001953125f);
+}
+
+// Magnitude of E2M1 index m (0..7): 0, .5, 1, 1.5, 2, 3, 4, 6 (exact bits).
+__device__ __forceinline__ float e2m1_mag(uint32_t m) {
+  uint32_t hi = m >> 1;
+  uint32_t bits = ((126u + hi) << 23) | ((hi ? (m & 1u) : 0u) << 22);
+  return m ? __uint_as_float(bits) : 0.0f;
+}
+
+// Signed value of a 4-bit code.
+__device__ __forceinline__ float e2m1_value(uint32_t code) {
+  float v = e2m1_mag(code & 7u);
+  return (code & 8u) ? -v : v;
+}
+
+// Stochastic rounding of q to a 4-bit code with a 16-bit uniform number:
+// neighbours lo <= |q| < hi on the grid, frac = (|q| - lo) / (hi - lo)
+// (exact), round up iff u16 < fl(frac * 65536); |q| >= 6 saturates.
+__device__ __forceinline__ uint32_t e2m1_sr(float q, uint32_t u16) {
+  uint32_t sign = (__float_as_uint(q) >> 28) & 8u;
+  float a = fabsf(q);
+  if (!(a < 6.0f)) return sign | 7u;
+  uint32_t lo = (a >= 0.5f) + (a >= 1.0f) + (a >= 1.5f) + (a >= 2.0f) + (a >= 3.0f) + (a >= 4.0f);
+  float flo = e2m1_mag(lo), fhi = e2m1_mag(lo + 1);
+  float frac = __fdiv_rn(__fsub_rn(a, flo), __fsub_rn(fhi, flo));
+  float thr = __fmul_rn(frac, 65536.0f);
+  uint32_t up = __uint2float_rn(u16) < thr;
+  return sign | (lo + up);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// --------------------------------------------------------------------------
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): the published round
+// multipliers and Weyl key increments.
+// --------------------------------------------------------------------------
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int i = 0; i < 10; ++i) {
+    uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
+    uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return c;
+}
+
+// The 16 rounding draws of the 16 elements starting at output-orientation
+// linear index i0 (i0 % 16 == 0): element e draws half (e & 1) of word
+// (e % 8) / 2 of the call with counter i0 / 8 + e / 8.
+__device__ __forceinline__ void sr_draws16(uint64_t seed, uint64_t offset, uint64_t i0, uint32_t u[16]) {
+  uint64_t j = i0 >> 3;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint64_t jj = j + h;
+    uint4 w = philox4x32_10(make_uint4((uint32_t)jj, (uint32_t)(jj >> 32), (uint32_t)offset, (uint32_t)(offset >> 32)),
+                            (uint32_t)seed, (uint32_t)(seed >> 32));
+    u[8 * h + 0] = w.x & 0xFFFFu; u[8 * h + 1] = w.x >> 16;
+    u[8 * h + 2] = w.y & 0xFFFFu; u[8 * h + 3] = w.y >> 16;
+    u[8 * h + 4] = w.z & 0xFFFFu; u[8 * h + 5] = w.z >> 16;
+    u[8 * h + 6] = w.w & 0xFFFFu; u[8 * h + 7] = w.w >> 16;
+  }
+}
+
+// Sign mask of the Hadamard transform: bit i set -> sigma_i = -1.
+__device__ __forceinline__ uint32_t rht_sign_mask(uint64_t rht_seed) {
+  uint4 w = philox4x32_10(make_uint4(0u, 0x80000000u, 0u, 0u), (uint32_t)rht_seed, (uint32_t)(rht_seed >> 32));
+  return w.x & 0xFFFFu;
+}
+
+// v <- 1/4 * H16 * diag(sigma) * v, fast Walsh-Hadamard butterfly in fp32
+// (Sylvester order), then the exact 1/4.
+__device__ __forceinline__ void rht16(float v[16], uint32_t sign_mask) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = ((sign_mask >> i) & 1u) ? -v[i] : v[i];
+#pragma unroll
+  for (int h = 1; h < 16; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 16; i += 2 * h) {
+#pragma unroll
+      for (int j = i; j < i + h; ++j) {
+        float a = v[j], b = v[j + h];
+        v[j] = __fadd_rn(a, b);
+        v[j + h] = __fsub_rn(a, b);
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __fmul_rn(v[i], 0.25f);
+}
+
+// --------------------------------------------------------------------------
+// Scale factors
+// --------------------------------------------------------------------------
+
+// Byte offset of logical scale (r, kb) in the 128x4-atom layout; n_katoms =
+// ceil(K / 64).
+__device__ __forceinline__ int64_t sf_offset(int64_t r, int64_t kb, int64_t n_katoms) {
+  return ((r >> 7) * n_katoms + (kb >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (kb & 3);
+}
+
+// Per-tensor decode scale g = fl(amax / 2688), 1 for an all-zero tensor.
+__device__ __forceinline__ float global_scale(float amax) { return amax == 0.0f ? 1.0f : __fdiv_rn(amax, 2688.0f); }
+
+// One candidate block scale for grid maximum m: returns the E4M3 byte and
+// sets its value s, the decode scale S = fl(s*g) and r = fl(1/S) (0 if S = 0).
+__device__ __forceinline__ uint32_t block_scale(float amax_b, float mg, float g, float& s, float& rcp) {
+  uint32_t b = e4m3_rne_sat(__fdiv_rn(amax_b, mg));
+  s = e4m3_value(b);
+  float S = __fmul_rn(s, g);
+  rcp = (S == 0.0f) ? 0.0f : __frcp_rn(S);
+  return b;
+}
+
+// Encode 16 values with block reciprocal rcp into two 32-bit words of codes.
+template <bool SR>
+__device__ __forceinline__ uint2 encode16(const float v[16], float rcp, const uint32_t* u) {
+  float q[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) q[i] = __fmul_rn(v[i], rcp);
+  if constexpr (!SR) {
+    return make_uint2(e2m1x8_rne(q), e2m1x8_rne(q + 8));
+  } else {
+    uint32_t w0 = 0, w1 = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w0 |= e2m1_sr(q[i], u[i]) << (4 * i);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w1 |= e2m1_sr(q[8 + i], u[8 + i]) << (4 * i);
+    return make_uint2(w0, w1);
+  }
+}
+
+// Squared error of 16 encoded values against their decode fl(fl(v*s)*g),
+// pairwise summed: ((e0+e1)+(e2+e3)) + ... over the 16 in order.
+__device__ __forceinline__ float block_sq_err16(const float v[16], uint2 codes, float s, float g) {
+  float e[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    uint32_t c = ((i < 8 ? codes.x : codes.y) >> (4 * (i & 7))) & 15u;
+    float deq = __fmul_rn(__fmul_rn(e2m1_value(c), s), g);
+    float d = __fsub_rn(v[i], deq);
+    e[i] = __fmul_rn(d, d);
+  }
+#pragma unroll
+  for (int w = 1; w < 16; w <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 16; i += 2 * w) e[i] = __fadd_rn(e[i], e[i + w]);
+  }
+  return e[0];
+}
+
+}  // namespace nvfp4

@@ -1,0 +1,508 @@
+// NVFP4 quantizer kernels for sm_103a: tensor amax, row-wise (K = cols)
+// and transposed (K = rows) encoders with 1D/2D blocks, stochastic rounding,
+// Four-over-Six and the 16x16 Random Hadamard Transform, and the decoder.
+//
+// Format and recipe: "NVIDIA Introduces a 4-Bit Pretraining Methodology Using
+// NVFP4" ("Summary": 16-element blocks, E4M3 block scales, FP32 tensor scale;
+// "Method": 2D 16x16 weight blocks, RHT on Wgrad inputs, SR on gradients);
+// Four-over-Six: the hyper.ai story on the Nemotron 3 Ultra NVFP4 checkpoint.
+//
+// All kernels are HBM-bound.  Each CTA of an encoder owns one 128-row x
+// 4-block tile of the output orientation, i.e. exactly one 512-byte atom of
+// the scale layout, so every scale byte (padding included) is written by the
+// encoder and no memset is needed.  Loads are 16-byte vectors; the transposed
+// encoder stages a 64 x 128 input tile in shared memory and reads it back as
+// column pairs (32-bit words), conflict-free.
+#include "nvfp4_device.cuh"
+#include "quantize.h"
+
+namespace nvfp4 {
+
+// ---------------------------------------------------------------------------
+// Tensor amax: max |x| as the max of the magnitude bit patterns (non-negative
+// floats order like unsigned integers), one atomicMax per CTA.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t absmax_bits(uint4 w, float) {
+  uint32_t a = max(w.x & 0x7FFFFFFFu, w.y & 0x7FFFFFFFu);
+  uint32_t b = max(w.z & 0x7FFFFFFFu, w.w & 0x7FFFFFFFu);
+  return max(a, b);
+}
+__device__ __forceinline__ uint32_t absmax_bits(uint4 w, __nv_bfloat16) {
+  uint32_t m = __vmaxu2(__vmaxu2(w.x & 0x7FFF7FFFu, w.y & 0x7FFF7FFFu), __vmaxu2(w.z & 0x7FFF7FFFu, w.w & 0x7FFF7FFFu));
+  return max(m & 0xFFFFu, m >> 16) << 16;
+}
+
+__device__ __forceinline__ void cta_max_to_global(uint32_t m, unsigned int* out) {
+  __shared__ uint32_t red[32];
+  m = __reduce_max_sync(0xFFFFFFFFu, m);
+  int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) red[warp] = m;
+  __syncthreads();
+  if (warp == 0) {
+    m = lane < (int)(blockDim.x >> 5) ? red[lane] : 0u;
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    if (lane == 0 && m) atomicMax(out, m);
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) k_amax(const T* __restrict__ x, int64_t rows, int64_t nvec, int64_t ld_vec,
+                                              unsigned int* __restrict__ out) {
+  const uint4* base = reinterpret_cast<const uint4*>(x);
+  uint32_t m = 0;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
+    const uint4* row = base + r * ld_vec;
+    int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (; v + 3 * stride < nvec; v += 4 * stride) {
+      uint4 a = __ldg(row + v), b = __ldg(row + v + stride), c = __ldg(row + v + 2 * stride),
+            d = __ldg(row + v + 3 * stride);
+      m = max(m, max(max(absmax_bits(a, T()), absmax_bits(b, T())), max(absmax_bits(c, T()), absmax_bits(d, T()))));
+    }
+    for (; v < nvec; v += stride) m = max(m, absmax_bits(__ldg(row + v), T()));
+  }
+  cta_max_to_global(m, out);
+}
+
+// ---------------------------------------------------------------------------
+// Shared encode step for one thread's two blocks.
+// ---------------------------------------------------------------------------
+template <typename T>
+__device__ __forceinline__ void load16(const T* p, float v[16]);
+template <>
+__device__ __forceinline__ void load16<__nv_bfloat16>(const __nv_bfloat16* p, float v[16]) {
+  const uint4* q = reinterpret_cast<const uint4*>(p);
+  uint4 a = __ldg(q), b = __ldg(q + 1);
+  uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    v[2 * i] = bf16_lo(w[i]);
+    v[2 * i + 1] = bf16_hi(w[i]);
+  }
+}
+template <>
+__device__ __forceinline__ void load16<float>(const float* p, float v[16]) {
+  const float4* q = reinterpret_cast<const float4*>(p);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float4 f = __ldg(q + i);
+    v[4 * i] = f.x; v[4 * i + 1] = f.y; v[4 * i + 2] = f.z; v[4 * i + 3] = f.w;
+  }
+}
+
+__device__ __forceinline__ float absmax16(const float v[16]) {
+  float m = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(v[i]));
+  return m;
+}
+
+// ---------------------------------------------------------------------------
+// Row-wise encoder: K = cols.  Thread t of the 256 owns blocks
+// (row R0 + t/4 + 64h, block KB0 + t%4), h = 0, 1.  A 2D tile's 16 rows are the
+// 8-row groups of warps 2i and 2i+1 (lane bits 2..4 = row bits 0..2).
+// ---------------------------------------------------------------------------
+template <typename T, bool B2D, bool SR, bool F46, bool RHT, bool AMAX_ONLY>
+__global__ void __launch_bounds__(256) k_quant_rows(QuantArgs a) {
+  __shared__ float xw[8][2][4];    // cross-warp exchange for 2D tiles
+  __shared__ float xw4[8][2][4];
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int kbl = t & 3, rl = t >> 2;
+  const int64_t KB = a.K / 16, nka = (KB + 3) / 4;
+  const int64_t kb = (int64_t)blockIdx.x * 4 + kbl;
+  uint32_t mask = 0;
+  if constexpr (RHT) mask = rht_sign_mask(a.rht_seed);
+
+  float v[2][16];
+  bool valid[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    int64_t r = (int64_t)blockIdx.y * 128 + rl + 64 * h;
+    valid[h] = r < a.R && kb < KB;
+    if (valid[h]) {
+      load16<T>(reinterpret_cast<const T*>(a.x) + r * a.ld + kb * 16, v[h]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[h][i] = 0.0f;
+    }
+    if constexpr (RHT) rht16(v[h], mask);
+  }
+
+  if constexpr (AMAX_ONLY) {
+    uint32_t m = __float_as_uint(fmaxf(absmax16(v[0]), absmax16(v[1])));
+    cta_max_to_global(m, reinterpret_cast<unsigned int*>(a.amax_accum));
+    return;
+  } else {
+    const float amax = *a.amax_in;
+    const float g = global_scale(amax);
+    if (blockIdx.x == 0 && blockIdx.y == 0 && t == 0) {
+      *a.g_out = g;
+      if (a.amax_out != a.amax_in) *a.amax_out = amax;
+    }
+    float ab[2] = {absmax16(v[0]), absmax16(v[1])};
+    if constexpr (B2D) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float m = ab[h];
+        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
+        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 8));
+        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 16));
+        if (lane < 4) xw[warp][h][kbl] = m;
+        ab[h] = m;
+      }
+      __syncthreads();
+#pragma unroll
+      for (int h = 0; h < 2; ++h) ab[h] = fmaxf(ab[h], xw[warp ^ 1][h][kbl]);
+    }
+    const float g6 = __fmul_rn(6.0f, g), g4 = __fmul_rn(4.0f, g);
+    uint2 codes[2];
+    uint32_t sbyte[2];
+    uint32_t u[2][16];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      int64_t r = (int64_t)blockIdx.y * 128 + rl + 64 * h;
+      if constexpr (SR) sr_draws16(a.seed, a.offset, (uint64_t)(r * a.K + kb * 16), u[h]);
+      float s6, r6;
+      sbyte[h] = block_scale(ab[h], g6, g, s6, r6);
+      codes[h] = encode16<SR>(v[h], r6, u[h]);
+      if constexpr (F46) {
+        float s4, r4;
+        uint32_t b4 = block_scale(ab[h], g4, g, s4, r4);
+        uint2 c4 = encode16<SR>(v[h], r4, u[h]);
+        float e6 = block_sq_err16(v[h], codes[h], s6, g);
+        float e4 = block_sq_err16(v[h], c4, s4, g);
+        if constexpr (B2D) {
+#pragma unroll
+          for (int o = 4; o <= 16; o <<= 1) {
+            e6 = __fadd_rn(e6, __shfl_xor_sync(0xFFFFFFFFu, e6, o));
+            e4 = __fadd_rn(e4, __shfl_xor_sync(0xFFFFFFFFu, e4, o));
+          }
+          __syncthreads();  // xw reuse: every thread has read the amax exchange
+          if (lane < 4) {
+            xw[warp][h][kbl] = e6;
+            xw4[warp][h][kbl] = e4;
+          }
+          __syncthreads();
+          // tile sum = rows 0..7 + rows 8..15 (lower warp first; fp add commutes)
+          e6 = __fadd_rn(e6, xw[warp ^ 1][h][kbl]);
+          e4 = __fadd_rn(e4, xw4[warp ^ 1][h][kbl]);
+        }
+        if (e4 < e6) {
+          codes[h] = c4;
+          sbyte[h] = b4;
+        }
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      int64_t r = (int64_t)blockIdx.y * 128 + rl + 64 * h;
+      if (valid[h]) {
+        *reinterpret_cast<uint2*>(a.codes + r * (a.K / 2) + kb * 8) = codes[h];
+        if (a.tdebug) {
+          float4* d = reinterpret_cast<float4*>(a.tdebug + r * a.K + kb * 16);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) d[i] = make_float4(v[h][4 * i], v[h][4 * i + 1], v[h][4 * i + 2], v[h][4 * i + 3]);
+        }
+      }
+      a.scales[sf_offset(r, kb, nka)] = valid[h] ? (uint8_t)sbyte[h] : (uint8_t)0;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Transposed encoder: x is [Tt][N] row-major, the output orientation is
+// N x Tt (K = Tt).  A CTA stages 64 input rows x 128 columns in shared memory;
+// thread t then owns output rows n0 + 2*(t%64) + {0, 1} and block t/64 of the
+// tile (16 consecutive input rows).  A 2D tile (16 output rows) is 8
+// consecutive lanes (lane bits 0..2 = row-pair bits).
+// ---------------------------------------------------------------------------
+template <typename T>
+struct ColTile;
+template <>
+struct ColTile<__nv_bfloat16> {
+  static constexpr int kRowBytes = 256;  // 128 columns
+  __device__ static void pair(const uint8_t* s, int tok, int np, float& lo, float& hi) {
+    uint32_t w = reinterpret_cast<const uint32_t*>(s + tok * kRowBytes)[np];
+    lo = bf16_lo(w);
+    hi = bf16_hi(w);
+  }
+};
+template <>
+struct ColTile<float> {
+  static constexpr int kRowBytes = 512;
+  __device__ static void pair(const uint8_t* s, int tok, int np, float& lo, float& hi) {
+    float2 f = reinterpret_cast<const float2*>(s + tok * kRowBytes)[np];
+    lo = f.x;
+    hi = f.y;
+  }
+};
+
+template <typename T, bool B2D, bool SR, bool F46, bool RHT, bool AMAX_ONLY>
+__global__ void __launch_bounds__(256) k_quant_cols(QuantArgs a) {
+  constexpr int RB = ColTile<T>::kRowBytes;
+  __shared__ __align__(16) uint8_t tile[64 * RB];
+  const int t = threadIdx.x, lane = t & 31;
+  const int64_t Tt = a.R_in, N = a.C_in;  // input rows / cols
+  const int64_t K = Tt, KB = K / 16, nka = (KB + 3) / 4;
+  const int64_t tok0 = (int64_t)blockIdx.y * 64, n0 = (int64_t)blockIdx.x * 128;
+
+  // stage the input tile (rows beyond Tt or columns beyond N read as zero)
+  constexpr int VPR = RB / 16;  // 16-byte vectors per tile row
+#pragma unroll
+  for (int i = 0; i < (64 * VPR) / 256; ++i) {
+    int idx = t + 256 * i, row = idx / VPR, cv = idx % VPR;
+    int64_t col = n0 + (int64_t)cv * (16 / sizeof(T));
+    uint4 w = make_uint4(0, 0, 0, 0);
+    if (tok0 + row < Tt && col < N)
+      w = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(a.x) + (tok0 + row) * a.ld + col));
+    *reinterpret_cast<uint4*>(tile + row * RB + cv * 16) = w;
+  }
+  __syncthreads();
+
+  const int np = t & 63, kbl = t >> 6;
+  const int64_t kb = (int64_t)blockIdx.y * 4 + kbl;
+  uint32_t mask = 0;
+  if constexpr (RHT) mask = rht_sign_mask(a.rht_seed);
+  float v[2][16];
+#pragma unroll
+  for (int e = 0; e < 16; ++e) ColTile<T>::pair(tile, 16 * kbl + e, np, v[0][e], v[1][e]);
+  if constexpr (RHT) {
+    rht16(v[0], mask);
+    rht16(v[1], mask);
+  }
+  bool valid[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) valid[h] = (n0 + 2 * np + h < N) && kb < KB;
+
+  if constexpr (AMAX_ONLY) {
+    uint32_t m = __float_as_uint(fmaxf(absmax16(v[0]), absmax16(v[1])));
+    cta_max_to_global(m, reinterpret_cast<unsigned int*>(a.amax_accum));
+    return;
+  } else {
+    const float amax = *a.amax_in;
+    const float g = global_scale(amax);
+    if (blockIdx.x == 0 && blockIdx.y == 0 && t == 0) {
+      *a.g_out = g;
+      if (a.amax_out != a.amax_in) *a.amax_out = amax;
+    }
+    float ab[2] = {absmax16(v[0]), absmax16(v[1])};
+    if constexpr (B2D) {
+      float m = fmaxf(ab[0], ab[1]);
+      m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+      m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+      m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
+      ab[0] = ab[1] = m;
+    }
+    const float g6 = __fmul_rn(6.0f, g), g4 = __fmul_rn(4.0f, g);
+    uint2 codes[2], c4[2];
+    uint32_t sbyte[2], b4[2];
+    float e6[2], e4[2];
+    uint32_t u[2][16];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      int64_t n = n0 + 2 * np + h;
+      if constexpr (SR) sr_draws16(a.seed, a.offset, (uint64_t)(n * K + kb * 16), u[h]);
+      float s6, r6;
+      sbyte[h] = block_scale(ab[h], g6, g, s6, r6);
+      codes[h] = encode16<SR>(v[h], r6, u[h]);
+      if constexpr (F46) {
+        float s4, r4;
+        b4[h] = block_scale(ab[h], g4, g, s4, r4);
+        c4[h] = encode16<SR>(v[h], r4, u[h]);
+        e6[h] = block_sq_err16(v[h], codes[h], s6, g);
+        e4[h] = block_sq_err16(v[h], c4[h], s4, g);
+      }
+    }
+    if constexpr (F46) {
+      if constexpr (B2D) {
+        // tile rows 2p, 2p+1 are this thread's pair; then pairs of pairs ...
+        float s6 = __fadd_rn(e6[0], e6[1]), s4 = __fadd_rn(e4[0], e4[1]);
+#pragma unroll
+        for (int o = 1; o <= 4; o <<= 1) {
+          s6 = __fadd_rn(s6, __shfl_xor_sync(0xFFFFFFFFu, s6, o));
+          s4 = __fadd_rn(s4, __shfl_xor_sync(0xFFFFFFFFu, s4, o));
+        }
+        e6[0] = e6[1] = s6;
+        e4[0] = e4[1] = s4;
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+        if (e4[h] < e6[h]) {
+          codes[h] = c4[h];
+          sbyte[h] = b4[h];
+        }
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      int64_t n = n0 + 2 * np + h;
+      if (valid[h]) {
+        *reinterpret_cast<uint2*>(a.codes + n * (K / 2) + kb * 8) = codes[h];
+        if (a.tdebug) {
+          float4* d = reinterpret_cast<float4*>(a.tdebug + n * K + kb * 16);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) d[i] = make_float4(v[h][4 * i], v[h][4 * i + 1], v[h][4 * i + 2], v[h][4 * i + 3]);
+        }
+      }
+      a.scales[sf_offset(n, kb, nka)] = valid[h] ? (uint8_t)sbyte[h] : (uint8_t)0;
+    }
+    (void)lane;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Decoder: one thread per block of 16 (grid-stride).
+// ---------------------------------------------------------------------------
+template <typename TO>
+__global__ void __launch_bounds__(256) k_dequant(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales,
+                                                 const float* __restrict__ gptr, int64_t R, int64_t K, TO* __restrict__ y) {
+  const float g = *gptr;
+  const int64_t KB = K / 16, nka = (KB + 3) / 4, nblk = R * KB;
+  for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < nblk; b += (int64_t)gridDim.x * blockDim.x) {
+    int64_t r = b / KB, kb = b % KB;
+    uint2 c = *reinterpret_cast<const uint2*>(codes + r * (K / 2) + kb * 8);
+    float s = e4m3_value(scales[sf_offset(r, kb, nka)] & 0x7Fu);
+    float o[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      uint32_t code = ((i < 8 ? c.x : c.y) >> (4 * (i & 7))) & 15u;
+      o[i] = __fmul_rn(__fmul_rn(e2m1_value(code), s), g);
+    }
+    if constexpr (sizeof(TO) == 4) {
+      float4* d = reinterpret_cast<float4*>(y + r * K + kb * 16);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) d[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+    } else {
+      uint32_t w[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        __nv_bfloat162 p = __floats2bfloat162_rn(o[2 * i], o[2 * i + 1]);
+        w[i] = *reinterpret_cast<uint32_t*>(&p);
+      }
+      uint4* d = reinterpret_cast<uint4*>(y + r * K + kb * 16);
+      d[0] = make_uint4(w[0], w[1], w[2], w[3]);
+      d[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    }
+  }
+}
+
+// Empty tensor: amax = 0, g = 1.
+__global__ void k_empty_scalars(float* amax, float* g) {
+  *amax = 0.0f;
+  *g = 1.0f;
+}
+
+// ---------------------------------------------------------------------------
+// Launchers
+// ---------------------------------------------------------------------------
+static int num_sms() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
+cudaError_t launch_amax(const void* x, bool bf16, int64_t rows, int64_t cols, int64_t ld, float* amax_accum,
+                        cudaStream_t s) {
+  const int64_t vec = bf16 ? 8 : 4;
+  int64_t r = rows, nvec = cols / vec, ldv = ld / vec;
+  if (ld == cols) {  // contiguous: one flat row
+    nvec = rows * cols / vec;
+    r = 1;
+    ldv = 0;
+  }
+  if (nvec == 0 || r == 0) return cudaSuccess;
+  int64_t want = (nvec + 1023) / 1024;
+  int64_t cap = (int64_t)num_sms() * 8;
+  unsigned gx = (unsigned)(want < 1 ? 1 : (want > cap ? cap : want));
+  unsigned gy = (unsigned)(r > 65535 ? 65535 : r);
+  if (gy > 1 && gx * gy > (unsigned)cap) gx = (unsigned)((cap + gy - 1) / gy);
+  dim3 grid(gx ? gx : 1, gy);
+  if (bf16)
+    k_amax<__nv_bfloat16><<<grid, 256, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(x), r, nvec, ldv,
+                                              reinterpret_cast<unsigned int*>(amax_accum));
+  else
+    k_amax<float><<<grid, 256, 0, s>>>(reinterpret_cast<const float*>(x), r, nvec, ldv,
+                                      reinterpret_cast<unsigned int*>(amax_accum));
+  return cudaGetLastError();
+}
+
+template <typename T, bool B2D, bool SR, bool F46, bool RHT, bool AO>
+static void launch_q(const QuantArgs& a, bool transpose, cudaStream_t s) {
+  if (!transpose) {
+    dim3 grid((unsigned)((a.K / 16 + 3) / 4), (unsigned)((a.R + 127) / 128));
+    k_quant_rows<T, B2D, SR, F46, RHT, AO><<<grid, 256, 0, s>>>(a);
+  } else {
+    dim3 grid((unsigned)((a.C_in + 127) / 128), (unsigned)((a.R_in + 63) / 64));
+    k_quant_cols<T, B2D, SR, F46, RHT, AO><<<grid, 256, 0, s>>>(a);
+  }
+}
+
+template <typename T, bool RHT, bool AO>
+static void dispatch_opts(const QuantArgs& a, bool transpose, bool b2d, bool sr, bool f46, cudaStream_t s) {
+  if (AO) {
+    launch_q<T, false, false, false, RHT, AO>(a, transpose, s);
+    return;
+  }
+  if (b2d) {
+    if (sr) {
+      if (f46) launch_q<T, true, true, true, RHT, AO>(a, transpose, s);
+      else launch_q<T, true, true, false, RHT, AO>(a, transpose, s);
+    } else {
+      if (f46) launch_q<T, true, false, true, RHT, AO>(a, transpose, s);
+      else launch_q<T, true, false, false, RHT, AO>(a, transpose, s);
+    }
+  } else {
+    if (sr) {
+      if (f46) launch_q<T, false, true, true, RHT, AO>(a, transpose, s);
+      else launch_q<T, false, true, false, RHT, AO>(a, transpose, s);
+    } else {
+      if (f46) launch_q<T, false, false, true, RHT, AO>(a, transpose, s);
+      else launch_q<T, false, false, false, RHT, AO>(a, transpose, s);
+    }
+  }
+}
+
+cudaError_t launch_quantize(const QuantArgs& a, bool bf16, bool transpose, bool b2d, bool sr, bool f46, bool rht,
+                            bool amax_only, cudaStream_t s) {
+  if (a.R == 0 || a.K == 0) return cudaSuccess;
+  if (bf16) {
+    if (rht) {
+      if (amax_only) dispatch_opts<__nv_bfloat16, true, true>(a, transpose, false, false, false, s);
+      else dispatch_opts<__nv_bfloat16, true, false>(a, transpose, false, sr, f46, s);
+    } else {
+      dispatch_opts<__nv_bfloat16, false, false>(a, transpose, b2d, sr, f46, s);
+    }
+  } else {
+    if (rht) {
+      if (amax_only) dispatch_opts<float, true, true>(a, transpose, false, false, false, s);
+      else dispatch_opts<float, true, false>(a, transpose, false, sr, f46, s);
+    } else {
+      dispatch_opts<float, false, false>(a, transpose, b2d, sr, f46, s);
+    }
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_empty_scalars(float* amax, float* g, cudaStream_t s) {
+  k_empty_scalars<<<1, 1, 0, s>>>(amax, g);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequantize(const uint8_t* codes, const uint8_t* scales, const float* g, int64_t R, int64_t K,
+                              void* y, bool bf16_out, cudaStream_t s) {
+  int64_t nblk = R * (K / 16);
+  if (nblk == 0) return cudaSuccess;
+  int64_t want = (nblk + 255) / 256, cap = (int64_t)num_sms() * 16;
+  unsigned grid = (unsigned)(want > cap ? cap : want);
+  if (bf16_out)
+    k_dequant<__nv_bfloat16><<<grid, 256, 0, s>>>(codes, scales, g, R, K, reinterpret_cast<__nv_bfloat16*>(y));
+  else
+    k_dequant<float><<<grid, 256, 0, s>>>(codes, scales, g, R, K, reinterpret_cast<float*>(y));
+  return cudaGetLastError();
+}
+
+}  // namespace nvfp4

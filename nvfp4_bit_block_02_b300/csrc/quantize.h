@@ -1,0 +1,31 @@
+// Internal launch interface of the quantizer kernels (not part of the C ABI).
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace nvfp4 {
+
+struct QuantArgs {
+  const void* x;        // input, row-major [R_in][ld]
+  int64_t R_in, C_in;   // input rows / cols
+  int64_t ld;           // input leading dimension (elements)
+  int64_t R, K;         // output orientation
+  const float* amax_in; // tensor amax the encoder uses
+  float* amax_out;      // copy of it (may alias amax_in)
+  float* amax_accum;    // atomicMax target of the amax-only passes
+  float* g_out;
+  uint8_t* codes;
+  uint8_t* scales;
+  float* tdebug;        // fp32 [R][K] transformed values, or nullptr
+  uint64_t seed, offset, rht_seed;
+};
+
+cudaError_t launch_amax(const void* x, bool bf16, int64_t rows, int64_t cols, int64_t ld, float* amax_accum,
+                        cudaStream_t s);
+cudaError_t launch_quantize(const QuantArgs& a, bool bf16, bool transpose, bool b2d, bool sr, bool f46, bool rht,
+                            bool amax_only, cudaStream_t s);
+cudaError_t launch_empty_scalars(float* amax, float* g, cudaStream_t s);
+cudaError_t launch_dequantize(const uint8_t* codes, const uint8_t* scales, const float* g, int64_t R, int64_t K,
+                              void* y, bool bf16_out, cudaStream_t s);
+
+}  // namespace nvfp4

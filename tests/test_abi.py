@@ -1,0 +1,120 @@
+"""The C-ABI library loads, exports every function include/nvfp4.h declares,
+and rejects bad arguments on the host before any launch (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import nvfp4_bit_block_02_b300 as nv
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "nvfp4.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from nvfp4_bit_block_02_b300 import build
+    build.build()
+    return nv.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(nvfp4_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ["nvfp4_quantize", "nvfp4_rht_quantize", "nvfp4_dequantize", "nvfp4_gemm",
+                     "nvfp4_gemm_grouped", "nvfp4_codes_bytes", "nvfp4_scales_bytes", "nvfp4_sync_check",
+                     "nvfp4_status_string", "nvfp4_last_error"]:
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+        assert ctypes.cast(getattr(L, name), ctypes.c_void_p).value
+
+
+def test_size_queries(L):
+    assert nv.codes_bytes(8192, 4096) == 8192 * 2048
+    assert nv.scales_bytes(8192, 4096) == 8192 * 256
+    assert nv.scales_bytes(130, 80) == 256 * 8         # rows padded to 128, blocks (5) to 4
+    assert nv.scales_bytes(0, 64) == 0 and nv.codes_bytes(0, 64) == 0
+
+
+def test_status_strings(L):
+    for code, name in nv.STATUS.items():
+        assert L.nvfp4_status_string(code).decode() == name
+
+
+def _fake_tensor(rows, cols, base=0x10000):
+    return nv.CTensor(base, base + 0x100000, base + 0x200000, base + 0x200100, rows, cols)
+
+
+def _call_quantize(L, x_ptr, dtype, rows, cols, ld, cfg, out):
+    return L.nvfp4_quantize(ctypes.c_void_p(x_ptr), dtype, rows, cols, ld, ctypes.byref(cfg), None,
+                            ctypes.byref(out), None)
+
+
+def test_quantize_argument_errors(L):
+    cfg = nv.CQuantConfig(nv.BLOCK_1D, nv.ROUND_RNE, nv.SCALE_MAX6, 0, 0, 0)
+    out = _fake_tensor(64, 64)
+    # bad dtype / enums
+    assert _call_quantize(L, 0x1000, 7, 64, 64, 64, cfg, out) == 1
+    bad = nv.CQuantConfig(5, 0, 0, 0, 0, 0)
+    assert _call_quantize(L, 0x1000, nv.BF16, 64, 64, 64, bad, out) == 1
+    # output orientation mismatch
+    assert _call_quantize(L, 0x1000, nv.BF16, 64, 64, 64, cfg, _fake_tensor(64, 32)) == 1
+    # K not a multiple of 16
+    assert _call_quantize(L, 0x1000, nv.BF16, 64, 40, 40, cfg, _fake_tensor(64, 40)) == 2
+    # 2D needs rows % 16
+    cfg2 = nv.CQuantConfig(nv.BLOCK_2D, 0, 0, 0, 0, 0)
+    assert _call_quantize(L, 0x1000, nv.BF16, 24, 64, 64, cfg2, _fake_tensor(24, 64)) == 2
+    # misaligned input / leading dimension
+    assert _call_quantize(L, 0x1008, nv.BF16, 64, 64, 64, cfg, out) == 3
+    assert _call_quantize(L, 0x1000, nv.BF16, 64, 64, 68, cfg, out) == 3
+    # NULL buffers
+    nul = nv.CTensor(0, 0x2000, 0x3000, 0x4000, 64, 64)
+    assert _call_quantize(L, 0x1000, nv.BF16, 64, 64, 64, cfg, nul) == 1
+    assert "codes" in L.nvfp4_last_error().decode()
+    # the RHT path refuses 2D blocks
+    assert L.nvfp4_rht_quantize(ctypes.c_void_p(0x1000), nv.BF16, 64, 64, 64, ctypes.byref(cfg2), 1, None,
+                                ctypes.byref(out), None, None) == 2
+
+
+def test_gemm_argument_errors(L):
+    A = _fake_tensor(128, 256)
+    B = _fake_tensor(256, 256, base=0x800000)
+    D = ctypes.c_void_p(0x4000000)
+    assert L.nvfp4_gemm(ctypes.byref(A), ctypes.byref(_fake_tensor(256, 512)), D, nv.BF16, 256, None) == 1
+    assert L.nvfp4_gemm(ctypes.byref(_fake_tensor(128, 128)), ctypes.byref(_fake_tensor(256, 128)), D, nv.BF16,
+                        256, None) == 2
+    assert L.nvfp4_gemm(ctypes.byref(_fake_tensor(100, 256)), ctypes.byref(B), D, nv.BF16, 256, None) == 2
+    assert L.nvfp4_gemm(ctypes.byref(A), ctypes.byref(B), D, nv.BF16, 200, None) == 1       # ldd < N
+    assert L.nvfp4_gemm(ctypes.byref(A), ctypes.byref(B), ctypes.c_void_p(0x4000008), nv.BF16, 256, None) == 3
+    assert L.nvfp4_gemm(ctypes.byref(A), ctypes.byref(B), D, 9, 256, None) == 1
+    assert L.nvfp4_gemm_grouped(nv.MAX_GROUPS + 1, None, None, None, nv.BF16, None) == 1
+    assert L.nvfp4_gemm_grouped(0, None, None, None, nv.BF16, None) == 0
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device error path")
+def test_launch_without_a_device_reports_cuda_error(L):
+    """With no GPU the first CUDA call fails; the API returns NVFP4_ERR_CUDA
+    with a message instead of crashing (the pointers are never touched)."""
+    cfg = nv.CQuantConfig(nv.BLOCK_1D, nv.ROUND_RNE, nv.SCALE_MAX6, 0, 0, 0)
+    out = _fake_tensor(64, 64)
+    st = _call_quantize(L, 0x1000, nv.BF16, 64, 64, 64, cfg, out)
+    assert st == 4
+    assert "cuda" in L.nvfp4_last_error().decode().lower()
+    assert L.nvfp4_sync_check(None) == 4
+
+
+def test_empty_tensors_are_ok_without_launch_for_gemm(L):
+    A = _fake_tensor(0, 256)
+    B = _fake_tensor(128, 256)
+    assert L.nvfp4_gemm(ctypes.byref(A), ctypes.byref(B), ctypes.c_void_p(0x4000000), nv.BF16, 128, None) == 0

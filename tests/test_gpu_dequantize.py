@@ -1,0 +1,46 @@
+"""Dequantizer parity on the GPU: fp32 output bit-exact with the oracle's
+y = fl(fl(value(code) * s_b) * g); BF16 output = that fp32 value rounded to
+nearest even."""
+import numpy as np
+import pytest
+import torch
+
+import nvfp4_bit_block_02_b300 as nv
+import oracle
+import synthetic
+from tests.gpu_helpers import oracle_quantize_like
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("shape", [(256, 256), (130, 80), (1, 16), (384, 1040)])
+@pytest.mark.parametrize("block", ["1d", "2d"])
+def test_dequantize_parity(shape, block):
+    rows, cols = shape
+    if block == "2d" and rows % 16:
+        pytest.skip("2D needs rows % 16")
+    x = torch.from_numpy(synthetic.with_entry_outliers(synthetic.normal(shape, 1.0, 50), 0.01, 50, 51))
+    q = nv.quantize(x.cuda(), block=block, scaling="four_over_six")
+    y32 = nv.dequantize(q, torch.float32)
+    y16 = nv.dequantize(q, torch.bfloat16)
+    nv.sync_check()
+    ref = oracle_quantize_like(x, block2d=block == "2d", four_over_six=True)
+    yr = oracle.dequantize(ref.codes, ref.scales, ref.g)
+    got = y32.cpu().numpy()
+    assert (got.view(np.uint32) == yr.view(np.uint32)).all()
+    assert torch.equal(y16.cpu(), torch.from_numpy(yr).to(torch.bfloat16))
+
+
+def test_dequantize_round_trip_of_grid_values():
+    """Values exactly on the grid of their block come back unchanged."""
+    rng = np.random.default_rng(7)
+    grid = np.array([0, .5, 1, 1.5, 2, 3, 4, 6], np.float32)
+    v = rng.choice(grid, size=(64, 256)) * rng.choice([-1, 1], size=(64, 256))
+    v[:, ::16] = 6.0
+    v[0, 1] = 2688.0 / 448 * 6 / 6   # keep amax = 6: g = 6/2688, S_b = 448 g = 1 in every block
+    x = torch.from_numpy(v.astype(np.float32))
+    q = nv.quantize(x.cuda())
+    y = nv.dequantize(q)
+    nv.sync_check()
+    ref = oracle_quantize_like(x)
+    assert (y.cpu().numpy() == oracle.dequantize(ref.codes, ref.scales, ref.g)).all()

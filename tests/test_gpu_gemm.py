@@ -1,0 +1,224 @@
+"""Block-scaled GEMM parity on the GPU against the oracle's float64 GEMM of
+the dequantized operands: |D - D_ref| <= 1e-5 * sum_k |a||b| (plus half a
+BF16 ulp of D_ref for BF16 output).  The operands are quantized on the GPU
+and first checked bit-exact against the oracle's quantization, so both sides
+multiply the same NVFP4 values."""
+import numpy as np
+import pytest
+import torch
+
+import nvfp4_bit_block_02_b300 as nv
+import oracle
+import synthetic
+from tests.gpu_helpers import assert_same_quantized, gemm_check, oracle_quantize_like
+
+pytestmark = pytest.mark.gpu
+
+
+def quantize_both(x_cpu, **kw):
+    q = nv.quantize(x_cpu.cuda(), **kw)
+    torch.cuda.synchronize()
+    okw = dict(transpose=kw.get("transpose", False), block2d=kw.get("block") == "2d",
+               stochastic=kw.get("rounding") == "stochastic", four_over_six=kw.get("scaling") == "four_over_six",
+               seed=kw.get("seed", 0), offset=kw.get("offset", 0))
+    ref = oracle_quantize_like(x_cpu, **okw)
+    assert_same_quantized(q, ref, "GEMM operand")
+    return q, ref
+
+
+def make_tensor_from_codes(codes: np.ndarray, logical_scales: np.ndarray, g: float) -> nv.NVFP4Tensor:
+    R, K2 = codes.shape
+    K = 2 * K2
+    phys = oracle.swizzle_scales(logical_scales, R, K)
+    return nv.NVFP4Tensor(torch.from_numpy(codes).cuda(), torch.from_numpy(phys).cuda(),
+                          torch.tensor([g], dtype=torch.float32, device="cuda"),
+                          torch.tensor([0.0], dtype=torch.float32, device="cuda"), R, K)
+
+
+def test_gemm_pr1_256():
+    wl = synthetic.pr1()
+    qa, ra = quantize_both(wl.tensors["A"])
+    qb, rb = quantize_both(wl.tensors["B"])
+    d = nv.gemm(qa, qb, out_dtype=torch.float32)
+    nv.sync_check()
+    ref, bound = oracle.gemm_reference(ra, rb)
+    gemm_check(d.cpu().numpy(), ref, bound, False, "PR1")
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 256), (256, 512, 512), (384, 384, 768), (128, 128, 256),
+                                   (512, 1280, 1024), (256, 256, 4096)])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_gemm_shapes(M, N, K, out_dtype):
+    a = torch.from_numpy(synthetic.normal((M, K), 1.0, M + K)).to(torch.bfloat16)
+    b = torch.from_numpy(synthetic.normal((N, K), 0.02, N + K + 1)).to(torch.bfloat16)
+    qa, ra = quantize_both(a)
+    qb, rb = quantize_both(b, block="2d")
+    d = nv.gemm(qa, qb, out_dtype=out_dtype)
+    nv.sync_check()
+    ref, bound = oracle.gemm_reference(ra, rb)
+    gemm_check(d.float().cpu().numpy(), ref, bound, out_dtype == torch.bfloat16, f"{M}x{N}x{K}")
+
+
+def test_gemm_all_ones_closed_form():
+    M, N, K = 128, 256, 512
+    a = make_tensor_from_codes(np.full((M, K // 2), 0x22, np.uint8), np.full((M, K // 16), 0x38, np.uint8), 1.0)
+    b = make_tensor_from_codes(np.full((N, K // 2), 0x22, np.uint8), np.full((N, K // 16), 0x38, np.uint8), 1.0)
+    d = nv.gemm(a, b, out_dtype=torch.float32)
+    nv.sync_check()
+    assert (d.cpu().numpy() == K).all()
+
+
+def test_gemm_exact_integer_products():
+    """Integer-valued codes, power-of-two scales, g = 1: the result is exact
+    in fp32, so the GPU must match the oracle exactly."""
+    rng = np.random.default_rng(5)
+    M, N, K = 256, 512, 512
+    ints = np.array([0, 2, 4, 5, 6, 7, 8, 10, 12, 13, 14, 15], np.uint8)
+    pack = lambda c: (c[:, 0::2] | (c[:, 1::2] << 4)).astype(np.uint8)
+    ca, cb = rng.choice(ints, (M, K)), rng.choice(ints, (N, K))
+    sa = rng.choice(np.array([0x30, 0x38, 0x40], np.uint8), (M, K // 16))   # 0.5, 1, 2
+    sb = rng.choice(np.array([0x30, 0x38, 0x40], np.uint8), (N, K // 16))
+    a = make_tensor_from_codes(pack(ca), sa, 1.0)
+    b = make_tensor_from_codes(pack(cb), sb, 1.0)
+    d = nv.gemm(a, b, out_dtype=torch.float32)
+    nv.sync_check()
+    ra = oracle.Quantized(pack(ca), sa, 0, 1.0, None, None, M, K)
+    rb = oracle.Quantized(pack(cb), sb, 0, 1.0, None, None, N, K)
+    ref, _ = oracle.gemm_reference(ra, rb)
+    got = d.cpu().numpy().astype(np.float64)
+    bad = np.argwhere(got != ref)
+    assert bad.size == 0, f"{len(bad)} differ; first {bad[:3].tolist()} {got[tuple(bad[0])]} vs {ref[tuple(bad[0])]}"
+
+
+def test_gemm_structured_scales_pin_the_layout():
+    """Every code 1.0; A's block scales are distinct powers of two per (row,
+    block) and B's per (column, block): each output is 16 * sum_kb sA * sB,
+    exact, and any misplaced scale byte changes it."""
+    rng = np.random.default_rng(6)
+    M, N, K = 256, 512, 1024
+    pows = np.array([0x28, 0x30, 0x38, 0x40, 0x48], np.uint8)   # 0.25 .. 4
+    sa = rng.choice(pows, (M, K // 16))
+    sb = rng.choice(pows, (N, K // 16))
+    a = make_tensor_from_codes(np.full((M, K // 2), 0x22, np.uint8), sa, 1.0)
+    b = make_tensor_from_codes(np.full((N, K // 2), 0x22, np.uint8), sb, 1.0)
+    d = nv.gemm(a, b, out_dtype=torch.float32)
+    nv.sync_check()
+    dec = np.vectorize(oracle.e4m3_decode)
+    ref = 16.0 * dec(sa).astype(np.float64) @ dec(sb).astype(np.float64).T
+    got = d.cpu().numpy().astype(np.float64)
+    bad = np.argwhere(got != ref)
+    assert bad.size == 0, f"{len(bad)} differ; first {bad[:3].tolist()}"
+
+
+def test_gemm_is_deterministic():
+    a = torch.from_numpy(synthetic.normal((256, 1024), 1.0, 40)).to(torch.bfloat16).cuda()
+    b = torch.from_numpy(synthetic.normal((512, 1024), 1.0, 41)).to(torch.bfloat16).cuda()
+    qa, qb = nv.quantize(a), nv.quantize(b)
+    outs = [nv.gemm(qa, qb) for _ in range(5)]
+    nv.sync_check()
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+
+
+def test_gemm_ldd_larger_than_n():
+    a = torch.from_numpy(synthetic.normal((128, 256), 1.0, 42)).to(torch.bfloat16)
+    b = torch.from_numpy(synthetic.normal((256, 256), 1.0, 43)).to(torch.bfloat16)
+    qa, ra = quantize_both(a)
+    qb, rb = quantize_both(b)
+    big = torch.full((128, 384), -7.0, dtype=torch.float32, device="cuda")
+    nv.gemm(qa, qb, out=big[:, :256])
+    nv.sync_check()
+    ref, bound = oracle.gemm_reference(ra, rb)
+    full = big.cpu().numpy()
+    gemm_check(full[:, :256], ref, bound, False, "ldd")
+    assert (full[:, 256:] == -7.0).all()
+
+
+def _sampled_check(qa_ref, qb_ref, d, bf16, rows, what):
+    ref, bound = oracle.gemm_reference(qa_ref, qb_ref, rows=rows)
+    return gemm_check(d[rows].float().cpu().numpy(), ref, bound, bf16, what)
+
+
+def test_gemm_llama8b_full_size_sampled():
+    wl = synthetic.llama8b_fprop()
+    qx, rx = quantize_both(wl.tensors["X"])
+    qw, rw = quantize_both(wl.tensors["W"], block="2d")
+    d = nv.gemm(qx, qw, out_dtype=torch.bfloat16)
+    nv.sync_check()
+    rng = np.random.default_rng(0)
+    rows = np.concatenate([np.arange(0, 128), np.arange(8064, 8192), rng.choice(8192, 64, replace=False)])
+    _sampled_check(rx, rw, d, True, rows, "8B fprop")
+
+
+def test_gemm_wgrad_full_size_sampled():
+    """dW = dY^T X with both operands RHT-transformed along the tokens, FP32 out."""
+    wl = synthetic.wgrad()
+    qd, _ = nv.rht_quantize(wl.tensors["dY"].cuda(), rht_seed=1, rounding="stochastic", seed=1)
+    qx, _ = nv.rht_quantize(wl.tensors["X"].cuda(), rht_seed=1)
+    d = nv.gemm(qd, qx, out_dtype=torch.float32)
+    nv.sync_check()
+    # the reference multiplies the GPU's own (separately verified) operands
+    rd = oracle.Quantized(qd.codes.cpu().numpy(), None, 0, float(qd.global_scale.cpu()[0]), None, None, qd.rows, qd.cols)
+    rx = oracle.Quantized(qx.codes.cpu().numpy(), None, 0, float(qx.global_scale.cpu()[0]), None, None, qx.rows, qx.cols)
+    rd.scales = _logical_from_physical(qd.scales.cpu().numpy(), qd.rows, qd.cols)
+    rx.scales = _logical_from_physical(qx.scales.cpu().numpy(), qx.rows, qx.cols)
+    rng = np.random.default_rng(1)
+    rows = np.concatenate([np.arange(0, 128), rng.choice(qd.rows, 64, replace=False)])
+    _sampled_check(rd, rx, d, False, rows, "wgrad")
+
+
+def _logical_from_physical(phys: np.ndarray, R: int, K: int) -> np.ndarray:
+    """Inverse of the documented scale layout (index arithmetic only)."""
+    KB = K // 16
+    nka = (KB + 3) // 4
+    r = np.arange(R)[:, None]
+    kb = np.arange(KB)[None, :]
+    off = ((r // 128) * nka + kb // 4) * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4 + kb % 4
+    return phys[off]
+
+
+def test_logical_from_physical_inverts_the_oracle_layout():
+    rng = np.random.default_rng(2)
+    R, K = 300, 1040
+    logical = rng.integers(1, 255, (R, K // 16), dtype=np.uint8)
+    assert (_logical_from_physical(oracle.swizzle_scales(logical, R, K), R, K) == logical).all()
+
+
+@pytest.mark.parametrize("groups", [1, 3, 70])
+def test_gemm_grouped_small(groups):
+    rng = np.random.default_rng(groups)
+    qa, qb, ra, rb = [], [], [], []
+    for e in range(groups):
+        M = int(rng.choice([128, 256]))
+        N = int(rng.choice([128, 256, 384]))
+        K = int(rng.choice([256, 512]))
+        a = torch.from_numpy(synthetic.normal((M, K), 1.0, 100 + e)).to(torch.bfloat16)
+        b = torch.from_numpy(synthetic.normal((N, K), 0.02, 200 + e)).to(torch.bfloat16)
+        x, y = quantize_both(a)
+        qa.append(x); ra.append(y)
+        x, y = quantize_both(b, block="2d")
+        qb.append(x); rb.append(y)
+    outs = nv.gemm_grouped(qa, qb, out_dtype=torch.bfloat16)
+    nv.sync_check()
+    for e in range(groups):
+        ref, bound = oracle.gemm_reference(ra[e], rb[e])
+        gemm_check(outs[e].float().cpu().numpy(), ref, bound, True, f"group {e}")
+
+
+def test_gemm_grouped_moe_full_size_sampled():
+    """64 experts: X_e (512 x 4096, max-6) times W_e^T (1536 x 4096,
+    Four-over-Six); every 8th expert checked on sampled rows."""
+    wl = synthetic.moe()
+    X, W = wl.tensors["X"], wl.tensors["W"]
+    qx = [nv.quantize(X[e].cuda()) for e in range(X.shape[0])]
+    qw = [nv.quantize(W[e].cuda(), transpose=True, scaling="four_over_six") for e in range(W.shape[0])]
+    outs = nv.gemm_grouped(qx, qw, out_dtype=torch.bfloat16)
+    nv.sync_check()
+    rng = np.random.default_rng(3)
+    for e in range(0, X.shape[0], 8):
+        rx = oracle_quantize_like(X[e])
+        rw = oracle_quantize_like(W[e], transpose=True, four_over_six=True)
+        assert_same_quantized(qx[e], rx, f"X_{e}")
+        assert_same_quantized(qw[e], rw, f"W_{e}")
+        rows = rng.choice(512, 32, replace=False)
+        _sampled_check(rx, rw, outs[e], True, rows, f"expert {e}")
