@@ -66,7 +66,8 @@ typedef enum { NVFP4_SCALE_MAX6 = 0, NVFP4_SCALE_FOUR_OVER_SIX = 1 } nvfp4_scali
  *          and holds entry (r, kb) at (r%32)*16 + ((r%128)/32)*4 + kb%4.
  *          Padding entries are written as 0 by the quantizer.
  *   global_scale device float[1]: g.
- *   amax   device float[1]: the tensor amax the encoder used. */
+ *   amax   device float[1]: the tensor amax the encoder used.
+ * codes and scales may be NULL when rows or cols is 0. */
 typedef struct {
   uint8_t* codes;
   uint8_t* scales;

@@ -31,8 +31,10 @@ int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 nvfp4_status check_tensor_buffers(const nvfp4_tensor* t, const char* name) {
   if (!t) return fail(NVFP4_ERR_INVALID_ARG, std::string(name) + " is NULL");
   if (t->rows < 0 || t->cols < 0) return fail(NVFP4_ERR_INVALID_ARG, std::string(name) + " has a negative size");
-  if (!t->codes || !t->scales || !t->global_scale || !t->amax)
-    return fail(NVFP4_ERR_INVALID_ARG, std::string(name) + " has a NULL buffer (codes, scales, global_scale, amax)");
+  if (!t->global_scale || !t->amax)
+    return fail(NVFP4_ERR_INVALID_ARG, std::string(name) + " has a NULL buffer (global_scale, amax)");
+  if ((!t->codes || !t->scales) && t->rows > 0 && t->cols > 0)
+    return fail(NVFP4_ERR_INVALID_ARG, std::string(name) + " has a NULL buffer (codes, scales)");
   if (!aligned16(t->codes) || !aligned16(t->scales))
     return fail(NVFP4_ERR_MISALIGNED, std::string(name) + " codes/scales must be 16-byte aligned");
   return NVFP4_OK;

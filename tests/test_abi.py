@@ -82,6 +82,8 @@ def test_quantize_argument_errors(L):
     nul = nv.CTensor(0, 0x2000, 0x3000, 0x4000, 64, 64)
     assert _call_quantize(L, 0x1000, nv.BF16, 64, 64, 64, cfg, nul) == 1
     assert "codes" in L.nvfp4_last_error().decode()
+    nul_g = nv.CTensor(0x2000, 0x2000, 0, 0x4000, 64, 64)
+    assert _call_quantize(L, 0x1000, nv.BF16, 64, 64, 64, cfg, nul_g) == 1
     # the RHT path refuses 2D blocks
     assert L.nvfp4_rht_quantize(ctypes.c_void_p(0x1000), nv.BF16, 64, 64, 64, ctypes.byref(cfg2), 1, None,
                                 ctypes.byref(out), None, None) == 2
