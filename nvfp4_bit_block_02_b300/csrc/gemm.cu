@@ -6,22 +6,35 @@
 // format of "NVIDIA Introduces a 4-Bit Pretraining Methodology Using NVFP4"
 // ("Summary").
 //
-// One CTA computes a 128 x 256 tile of D.  Warp roles:
-//   warp 0      TMA producer: A and B code tiles (128 B of K = 256 elements
-//               per row, 128B swizzle) by cp.async.bulk.tensor, the matching
-//               scale atoms (contiguous 512-byte atoms of the 128x4 scale
-//               layout) by cp.async.bulk, into a 4-stage ring.
-//   warp 1      owns the tensor memory (512 columns: the 256-column FP32
-//               accumulator and one scale-factor slot per stage) and issues,
-//               from one thread, tcgen05.cp of the scale atoms into TMEM and
-//               tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X
-//               (M = 128, N = 256, K = 64 per instruction).
-//   warps 2..5  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM
-//               lanes 32*(w%4)..+31 = tile rows), scale by g_A*g_B, convert,
-//               store.
-// Every mbarrier wait is bounded (kWaitLimitNs).  On expiry the CTA records
-// NVFP4 timeout in a device word, stops issuing, waits (bounded) for the
-// copies and MMAs it has in flight, frees its tensor memory and returns.
+// Persistent kernel, one CTA per SM, 128 x 256 output tiles in a grouped
+// raster order.  Warp roles (14 warps):
+//   warp 0       TMA producer: A and B code tiles (128 B of K = 256 elements
+//                per row, 128B swizzle) by cp.async.bulk.tensor and the
+//                matching 512-byte scale atoms by cp.async.bulk, into a
+//                3-stage shared-memory ring.
+//   warp 1       owns the tensor memory (512 columns: the 256-column FP32
+//                accumulator, then one scale slot per stage) and issues, from
+//                one thread, tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X
+//                (M = 128, N = 256, K = 64 per instruction).
+//   warps 2..5   scale warps: each owns one TMEM lane quarter and moves the
+//                stage's scale bytes from shared memory into the stage's scale
+//                slot with tcgen05.st.  For K-step j the MMA takes the 4 scales
+//                of row r from lane r % 32, column (scale address + r / 32), with
+//                scale address slot + 4j (A) and slot + 8j (B, 256 rows); lane l
+//                of quarter q holds the same words as lane l of quarter 0 (the
+//                layout tcgen05.cp .32x128b.warpx4 produces), so row l of each
+//                512-byte scale atom is one 16-byte load and four columns.  One
+//                16- (A) and one 32-column (B) store per warp and stage replace
+//                twelve tcgen05.cp, which occupied the tensor pipe longer than
+//                the MMAs themselves.
+//   warps 6..13  epilogue: two warps per lane quarter (128 columns each) drain
+//                the accumulator with tcgen05.ld, release it to the MMA warp,
+//                scale by g_A*g_B, convert, stage 32 x 128-byte boxes in
+//                swizzled shared memory and write them with TMA stores, while
+//                the next tile's mainloop runs.
+// Every mbarrier wait is bounded (kWaitLimitNs).  On expiry the CTA records a
+// timeout in a device word, every role leaves its loop, in-flight copies and
+// MMAs are waited for (bounded), tensor memory is freed and the kernel returns.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -35,33 +48,36 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BN = 256;
-#ifndef NVFP4_GEMM_MMA_N
-#define NVFP4_GEMM_MMA_N 256
-#endif
-constexpr int MMA_N = NVFP4_GEMM_MMA_N;
 constexpr int BKB = 128;  // bytes of K per stage per row = 256 FP4 elements
-constexpr int STAGES = 4;
+constexpr int STAGES = 3;
 constexpr int A_BYTES = BM * BKB;
 constexpr int B_BYTES = BN * BKB;
 constexpr int SFA_BYTES = 4 * 512;               // 4 K-atoms of the 128-row tile
 constexpr int SFB_BYTES = (BN / 128) * 4 * 512;  // per 128-row block of B
+constexpr int EPI_WARPS = 8;
+constexpr int EPI_BYTES = 32 * 128;              // one 32-row x 128-byte box per epilogue warp
 constexpr int OFF_A = 0;
 constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
 constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
 constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
-constexpr int OFF_BAR = OFF_SFB + STAGES * SFB_BYTES;
-constexpr int SMEM_BYTES = OFF_BAR + 128 + 1024;  // + barriers + alignment slack
+constexpr int OFF_EPI = OFF_SFB + STAGES * SFB_BYTES;
+constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * EPI_BYTES;
+constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;  // + barriers + alignment slack
 constexpr int TMEM_COLS = 512;
-constexpr int SF_COL0 = BN;                   // first scale-factor column
-constexpr int SF_COLS_PER_STAGE = 16 + 32;    // SFA 4 atoms x 4 cols, SFB 8 atoms x 4 cols
-constexpr int NUM_THREADS = 192;
+constexpr int SFA_COL0 = BN;                    // scale slots: SFA 16 columns per stage,
+constexpr int SFB_COL0 = BN + 64;               //              SFB 32 columns per stage (32-aligned)
+constexpr int NUM_WARPS = 2 + 4 + EPI_WARPS;
+constexpr int NUM_THREADS = 32 * NUM_WARPS;
+constexpr int GROUP_M = 16;                     // raster: 16 m-tiles per band
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
-static_assert(SF_COL0 + STAGES * SF_COLS_PER_STAGE <= TMEM_COLS, "TMEM budget");
+static_assert(SFA_COL0 + 16 * STAGES <= SFB_COL0 && SFB_COL0 + 32 * STAGES <= TMEM_COLS, "TMEM budget");
+static_assert(SFA_COL0 % 16 == 0 && SFB_COL0 % 32 == 0, "tcgen05.st .x16/.x32 need aligned columns");
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+static_assert(OFF_EPI % 1024 == 0 && OFF_B % 1024 == 0, "swizzled buffers need 1024-byte alignment");
 
 // instruction descriptor: E2M1 x E2M1 (kind::mxf4nvf4 encoding 1), UE4M3
 // scales, K-major A and B, dense K = 64, M and N fields.
-constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((uint32_t)(MMA_N >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -77,6 +93,9 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -91,20 +110,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 
 // Bounded wait: true when the phase completed; false on abort or timeout
 // (a timeout raises the CTA's abort flag and the device error word).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          unsigned int* err, unsigned long long limit = kWaitLimitNs) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, unsigned int* err) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = now_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (*abort_flag) return false;
-      if (now_ns() - t0 > limit) {
+      if (now_ns() - t0 > kWaitLimitNs) {
         *abort_flag = 1;
         atomicOr(err, 1u);
         return false;
       }
     }
+  }
+}
+
+// Short bounded wait used only on the way out.
+__device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
+  const unsigned long long t0 = now_ns();
+  while (!mbar_try_wait(bar, parity) && now_ns() - t0 < 100000000ull) {
   }
 }
 
@@ -114,6 +139,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(src)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
                "l"(src), "r"(bytes), "r"(bar)
@@ -125,9 +159,6 @@ __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
-__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
-}
 __device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t sfa, uint32_t sfb, uint32_t acc) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
@@ -136,16 +167,26 @@ __device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint3
       "l"(a), "l"(b), "r"(kIdesc), "r"(acc), "r"(sfa), "r"(sfb)
       : "memory");
 }
-
-// K-major operand tile, 128-byte rows, 128B swizzle: 8-row atoms of 1024 B.
-__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
-  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
-         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
 }
-// One 512-byte scale atom: 32 rows x 16 B, no swizzle, 8x16 B core matrices.
-__device__ __forceinline__ uint64_t desc_sf(uint32_t saddr) {
-  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(128 >> 4) << 32) | ((uint64_t)1 << 46);
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
+      "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
+      "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
 }
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 #define NVFP4_LD32(taddr, r)                                                                                         \
   asm volatile(                                                                                                      \
@@ -155,39 +196,90 @@ __device__ __forceinline__ uint64_t desc_sf(uint32_t saddr) {
         "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),     \
         "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),    \
         "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])                  \
-      : "r"(taddr))
+      : "r"(taddr)                                                                                                   \
+      : "memory")
 
-__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// K-major operand tile, 128-byte rows, 128B swizzle: 8-row atoms of 1024 B.
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
 
-struct TileJob {
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  __nv_bfloat162 p = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&p);
+}
+
+// One output tile and the operands it reads.
+struct Tile {
   const CUtensorMap* tmA;
   const CUtensorMap* tmB;
-  const uint8_t* sfa;  // scale buffer of A (128x4-atom layout)
+  const CUtensorMap* tmD;
+  const uint8_t* sfa;
   const uint8_t* sfb;
   const float* ga;
   const float* gb;
-  void* d;
-  int64_t ldd;
-  int M, N, K;
+  int N, K;
   int m_tile, n_tile;
 };
 
-// One 128 x 256 output tile; called by all 192 threads of the CTA.
-__device__ __forceinline__ void gemm_tile(const TileJob& j, bool out_bf16, uint8_t* smem, unsigned int* err) {
+// Raster order: bands of GROUP_M m-tiles; inside a band n-tiles advance
+// slowest, so the CTAs working at one time share A and B rows in L2.
+__device__ __forceinline__ void raster(int t, int mt, int nt, int& m_tile, int& n_tile) {
+  const int band_tiles = GROUP_M * nt;
+  const int band = t / band_tiles, in = t % band_tiles;
+  const int rows = min(GROUP_M, mt - band * GROUP_M);
+  m_tile = band * GROUP_M + in % rows;
+  n_tile = in / rows;
+}
+
+struct SingleSched {
+  const CUtensorMap* tmA;
+  const CUtensorMap* tmB;
+  const CUtensorMap* tmD;
+  const GemmArgs* a;
+  __device__ int num_tiles() const { return (a->M / BM) * ((a->N + BN - 1) / BN); }
+  __device__ Tile get(int t) const {
+    Tile x{tmA, tmB, tmD, a->sfa, a->sfb, a->ga, a->gb, a->N, a->K, 0, 0};
+    raster(t, a->M / BM, (a->N + BN - 1) / BN, x.m_tile, x.n_tile);
+    return x;
+  }
+};
+
+struct GroupedSched {
+  const GroupedArgs* g;
+  __device__ int num_tiles() const { return g->tile_start[g->count]; }
+  __device__ Tile get(int t) const {
+    int e = 0;
+    while (e + 1 < g->count && t >= g->tile_start[e + 1]) ++e;
+    Tile x{&g->tmA[e], &g->tmB[e], &g->tmD[e], g->sfa[e], g->sfb[e], g->ga[e], g->gb[e], g->N[e], g->K[e], 0, 0};
+    raster(t - g->tile_start[e], g->M[e] / BM, (g->N[e] + BN - 1) / BN, x.m_tile, x.n_tile);
+    return x;
+  }
+};
+
+template <class Sched>
+__device__ __forceinline__ void gemm_persistent(const Sched& sched, bool out_bf16, unsigned int* err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 1);
+  // barrier block: full[S], empty[S], sfready[S], accum_full, accum_empty, drain
+  const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * STAGES, sfr0 = empty0 + 8 * STAGES;
+  const uint32_t accum_full = sfr0 + 8 * STAGES, accum_empty = accum_full + 8, drain = accum_empty + 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 3);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES), accum = smem_u32(bars + 2 * STAGES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nk = j.K / 256;
-  const int64_t n_katoms = j.K / 64;
+  const int num_tiles = sched.num_tiles();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, 1);
+      mbar_init(sfr0 + 8 * s, 4);
     }
-    mbar_init(accum, 1);
+    mbar_init(accum_full, 1);
+    mbar_init(accum_empty, EPI_WARPS);
+    mbar_init(drain, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -202,111 +294,188 @@ __device__ __forceinline__ void gemm_tile(const TileJob& j, bool out_bf16, uint8
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // valid 128-row blocks of B in this tile (N % 128 == 0)
-  const int nb_valid = min(BN / 128, (j.N - j.n_tile * BN) / 128);
-  const uint32_t stage_tx = A_BYTES + B_BYTES + SFA_BYTES + nb_valid * 2048;
-
-  if (warp == 0 && lane == 0) {
-    // ---------------- producer ----------------
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(j.tmA)) : "memory");
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(j.tmB)) : "memory");
-    int issued = 0;
-    for (int kt = 0; kt < nk; ++kt) {
-      const int s = kt % STAGES;
-      const uint32_t ph = (kt / STAGES) & 1;
-      if (!mbar_wait(empty0 + 8 * s, ph ^ 1, abort_flag, err)) break;
-      const uint32_t fb = full0 + 8 * s;
-      mbar_expect_tx(fb, stage_tx);
-      tma_load_2d(smem_u32(smem + OFF_A + s * A_BYTES), j.tmA, kt * BKB, j.m_tile * BM, fb);
-      tma_load_2d(smem_u32(smem + OFF_B + s * B_BYTES), j.tmB, kt * BKB, j.n_tile * BN, fb);
-      bulk_g2s(smem_u32(smem + OFF_SFA + s * SFA_BYTES), j.sfa + ((int64_t)j.m_tile * n_katoms + 4 * kt) * 512,
-               SFA_BYTES, fb);
-      for (int nb = 0; nb < nb_valid; ++nb)
-        bulk_g2s(smem_u32(smem + OFF_SFB + s * SFB_BYTES + nb * 2048),
-                 j.sfb + ((int64_t)(j.n_tile * (BN / 128) + nb) * n_katoms + 4 * kt) * 512, 2048, fb);
-      issued = kt + 1;
-    }
-    if (*abort_flag) {
-      // let every copy this thread started land before the CTA exits
-      for (int kt = issued > STAGES ? issued - STAGES : 0; kt < issued; ++kt) {
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      uint32_t it = 0;
+      for (int t = blockIdx.x; t < num_tiles && !*abort_flag; t += gridDim.x) {
+        const Tile x = sched.get(t);
+        const int nk = x.K / 256;
+        const int64_t nka = x.K / 64;
+        const int nb_valid = min(BN / 128, (x.N - x.n_tile * BN) / 128);
+        const uint32_t tx = A_BYTES + B_BYTES + SFA_BYTES + nb_valid * 2048;
+        for (int kt = 0; kt < nk; ++kt, ++it) {
+          const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
+          if (!mbar_wait(empty0 + 8 * s, ph ^ 1, abort_flag, err)) break;
+          const uint32_t fb = full0 + 8 * s;
+          mbar_expect_tx(fb, tx);
+          tma_load_2d(smem_u32(smem + OFF_A + s * A_BYTES), x.tmA, kt * BKB, x.m_tile * BM, fb);
+          tma_load_2d(smem_u32(smem + OFF_B + s * B_BYTES), x.tmB, kt * BKB, x.n_tile * BN, fb);
+          bulk_g2s(smem_u32(smem + OFF_SFA + s * SFA_BYTES), x.sfa + ((int64_t)x.m_tile * nka + 4 * kt) * 512,
+                   SFA_BYTES, fb);
+          for (int nb = 0; nb < nb_valid; ++nb)
+            bulk_g2s(smem_u32(smem + OFF_SFB + s * SFB_BYTES + nb * 2048),
+                     x.sfb + ((int64_t)(x.n_tile * (BN / 128) + nb) * nka + 4 * kt) * 512, 2048, fb);
+        }
+      }
+      if (*abort_flag) {  // let copies already issued land before the CTA exits
         const unsigned long long t0 = now_ns();
-        while (!mbar_try_wait(full0 + 8 * (kt % STAGES), (kt / STAGES) & 1) && now_ns() - t0 < 100000000ull) {
+        while (now_ns() - t0 < 2000000ull) {
         }
       }
     }
-  } else if (warp == 1 && lane == 0) {
+  } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
-    for (int kt = 0; kt < nk; ++kt) {
-      const int s = kt % STAGES;
-      if (!mbar_wait(full0 + 8 * s, (kt / STAGES) & 1, abort_flag, err)) break;
-      tc_fence_after();
-      const uint32_t sfa_t = tmem + SF_COL0 + s * SF_COLS_PER_STAGE;
-      const uint32_t sfb_t = sfa_t + 16;
-      const uint32_t sa = smem_u32(smem + OFF_SFA + s * SFA_BYTES);
-      const uint32_t sb = smem_u32(smem + OFF_SFB + s * SFB_BYTES);
-#pragma unroll
-      for (int ka = 0; ka < 4; ++ka) {
-        tc_cp_sf(sfa_t + 4 * ka, desc_sf(sa + ka * 512));
-#pragma unroll
-        for (int nb = 0; nb < BN / 128; ++nb) tc_cp_sf(sfb_t + 8 * ka + 4 * nb, desc_sf(sb + nb * 2048 + ka * 512));
-      }
-      const uint32_t a0 = smem_u32(smem + OFF_A + s * A_BYTES);
-      const uint32_t b0 = smem_u32(smem + OFF_B + s * B_BYTES);
-#pragma unroll
-      for (int ka = 0; ka < 4; ++ka) {
-#pragma unroll
-        for (int nh = 0; nh < BN / MMA_N; ++nh) {
-          tc_mma(tmem + nh * MMA_N, desc_sw128(a0 + 32 * ka), desc_sw128(b0 + nh * MMA_N * BKB + 32 * ka),
-                 sfa_t + 4 * ka, sfb_t + 8 * ka + 4 * (nh * MMA_N / 128), (kt | ka) != 0);
-        }
-      }
-      tc_commit(empty0 + 8 * s);
-    }
-    tc_commit(accum);
-    if (*abort_flag) {
-      const unsigned long long t0 = now_ns();
-      while (!mbar_try_wait(accum, 0) && now_ns() - t0 < 100000000ull) {
-      }
-    }
-  } else if (warp >= 2) {
-    // ---------------- epilogue ----------------
-    const bool ok = mbar_wait(accum, 0, abort_flag, err);
-    tc_fence_after();
-    if (ok && !*abort_flag) {
-      const int q = warp & 3;
-      const int64_t row = (int64_t)j.m_tile * BM + q * 32 + lane;
-      const float alpha = __fmul_rn(*j.ga, *j.gb);
-      const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16);
-#pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        const int col0 = j.n_tile * BN + c * 32;
-        if (col0 >= j.N) break;  // warp-uniform
-        uint32_t r[32];
-        NVFP4_LD32(tbase + c * 32, r);
-        tmem_ld_wait();
-        if (out_bf16) {
-          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(j.d) + row * j.ldd + col0);
-#pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint32_t w[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              __nv_bfloat162 p = __floats2bfloat162_rn(__fmul_rn(alpha, __uint_as_float(r[8 * v + 2 * i])),
-                                                       __fmul_rn(alpha, __uint_as_float(r[8 * v + 2 * i + 1])));
-              w[i] = *reinterpret_cast<uint32_t*>(&p);
-            }
-            dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+    if (lane == 0) {
+      uint32_t it = 0, ti = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++ti) {
+        const Tile x = sched.get(t);
+        const int nk = x.K / 256;
+        if (!mbar_wait(accum_empty, (ti & 1) ^ 1, abort_flag, err)) break;
+        tc_fence_after();
+        for (int kt = 0; kt < nk; ++kt, ++it) {
+          const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
+          if (!mbar_wait(sfr0 + 8 * s, ph, abort_flag, err) || !mbar_wait(full0 + 8 * s, ph, abort_flag, err)) {
+            ok = false;
+            break;
           }
-        } else {
-          float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(j.d) + row * j.ldd + col0);
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(smem + OFF_A + s * A_BYTES);
+          const uint32_t b0 = smem_u32(smem + OFF_B + s * B_BYTES);
+          const uint32_t sfa = tmem + SFA_COL0 + 16 * s, sfb = tmem + SFB_COL0 + 32 * s;
 #pragma unroll
-          for (int v = 0; v < 8; ++v)
-            dst[v] = make_float4(__fmul_rn(alpha, __uint_as_float(r[4 * v])), __fmul_rn(alpha, __uint_as_float(r[4 * v + 1])),
-                                 __fmul_rn(alpha, __uint_as_float(r[4 * v + 2])),
-                                 __fmul_rn(alpha, __uint_as_float(r[4 * v + 3])));
+          for (int j = 0; j < 4; ++j)
+            tc_mma(tmem, desc_sw128(a0 + 32 * j), desc_sw128(b0 + 32 * j), sfa + 4 * j, sfb + 8 * j, (kt | j) != 0);
+          tc_commit(empty0 + 8 * s);
+        }
+        if (ok) tc_commit(accum_full);
+      }
+      tc_commit(drain);  // arrives when every MMA this thread issued has completed
+      mbar_drain(drain, 0);
+    }
+  } else if (warp < 6) {
+    // ---------------- scale warps: shared memory -> TMEM ----------------
+    const uint32_t q = warp & 3;
+    const uint32_t lane_base = (q * 32) << 16;
+    uint32_t it = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+      const Tile x = sched.get(t);
+      const int nk = x.K / 256;
+      for (int kt = 0; kt < nk; ++kt, ++it) {
+        const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
+        // warp vote: the tcgen05.st below is warp-collective
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(full0 + 8 * s, ph, abort_flag, err))) {
+          ok = false;
+          break;
+        }
+        // lane l: row l of every 512-byte atom = 16 bytes = 4 consecutive columns
+        const uint4* sa = reinterpret_cast<const uint4*>(smem + OFF_SFA + s * SFA_BYTES) + lane;
+        const uint4* sb = reinterpret_cast<const uint4*>(smem + OFF_SFB + s * SFB_BYTES) + lane;
+        uint32_t va[16], vb[32];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint4 wa = sa[j * 32];           // A atom j
+          const uint4 w0 = sb[j * 32];           // B rows 0..127, atom j
+          const uint4 w1 = sb[128 + j * 32];     // B rows 128..255, atom j
+          va[4 * j] = wa.x; va[4 * j + 1] = wa.y; va[4 * j + 2] = wa.z; va[4 * j + 3] = wa.w;
+          vb[8 * j] = w0.x; vb[8 * j + 1] = w0.y; vb[8 * j + 2] = w0.z; vb[8 * j + 3] = w0.w;
+          vb[8 * j + 4] = w1.x; vb[8 * j + 5] = w1.y; vb[8 * j + 6] = w1.z; vb[8 * j + 7] = w1.w;
+        }
+        tmem_st16(tmem + lane_base + SFA_COL0 + 16 * s, va);
+        tmem_st32(tmem + lane_base + SFB_COL0 + 32 * s, vb);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sfr0 + 8 * s);
+      }
+    }
+  } else {
+    // ---------------- epilogue ----------------
+    const int e = warp - 6;
+    const uint32_t q = warp & 3, half = e >> 2;
+    const uint32_t taddr0 = tmem + ((q * 32) << 16) + half * 128;
+    uint8_t* stage = smem + OFF_EPI + e * EPI_BYTES;
+    const uint32_t stage_u32 = smem_u32(stage);
+    uint32_t ti = 0;
+    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++ti) {
+      const Tile x = sched.get(t);
+      // warp vote: tcgen05.ld is warp-collective
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(accum_full, ti & 1, abort_flag, err))) break;
+      tc_fence_after();
+      const float alpha = __fmul_rn(*x.ga, *x.gb);
+      const int col0 = x.n_tile * BN + half * 128;
+      const int row0 = x.m_tile * BM + q * 32;
+      const bool active = col0 < x.N;  // warp-uniform (N % 128 == 0)
+      if (out_bf16) {
+        uint32_t pk[64];
+        if (active) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t r[32];
+            NVFP4_LD32(taddr0 + c * 32, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              pk[16 * c + i] = pack_bf16(__fmul_rn(alpha, __uint_as_float(r[2 * i])),
+                                         __fmul_rn(alpha, __uint_as_float(r[2 * i + 1])));
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(accum_empty);
+        if (active) {
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {  // 64 columns = one 128-byte box row
+            if (lane == 0) bulk_wait_read0();
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              *reinterpret_cast<uint4*>(stage + lane * 128 + ((i ^ (lane & 7)) << 4)) =
+                  make_uint4(pk[32 * cc + 4 * i], pk[32 * cc + 4 * i + 1], pk[32 * cc + 4 * i + 2], pk[32 * cc + 4 * i + 3]);
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(x.tmD, stage_u32, col0 + 64 * cc, row0);
+              bulk_commit();
+            }
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          if (active) {
+            NVFP4_LD32(taddr0 + c * 32, r);
+            tmem_ld_wait();
+          }
+          if (c == 3) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(accum_empty);
+          }
+          if (active) {
+            if (lane == 0) bulk_wait_read0();
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              *reinterpret_cast<float4*>(stage + lane * 128 + ((i ^ (lane & 7)) << 4)) =
+                  make_float4(__fmul_rn(alpha, __uint_as_float(r[4 * i])), __fmul_rn(alpha, __uint_as_float(r[4 * i + 1])),
+                              __fmul_rn(alpha, __uint_as_float(r[4 * i + 2])),
+                              __fmul_rn(alpha, __uint_as_float(r[4 * i + 3])));
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(x.tmD, stage_u32, col0 + 32 * c, row0);
+              bulk_commit();
+            }
+          }
         }
       }
     }
+    if (lane == 0) bulk_wait0();
+    __syncwarp();
   }
   tc_fence_before();
   __syncthreads();
@@ -317,26 +486,16 @@ __device__ __forceinline__ void gemm_tile(const TileJob& j, bool out_bf16, uint8
   }
 }
 
-__device__ __forceinline__ uint8_t* aligned_smem() {
-  extern __shared__ uint8_t smem_raw[];
-  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-}
-
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-    k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmArgs a) {
-  TileJob j{&tmA, &tmB, a.sfa, a.sfb, a.ga, a.gb, a.d, a.ldd, a.M, a.N, a.K, (int)blockIdx.y, (int)blockIdx.x};
-  gemm_tile(j, a.out_bf16 != 0, aligned_smem(), a.err);
+    k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+           const __grid_constant__ CUtensorMap tmD, const __grid_constant__ GemmArgs a) {
+  SingleSched s{&tmA, &tmB, &tmD, &a};
+  gemm_persistent(s, a.out_bf16 != 0, a.err);
 }
 
 __global__ void __launch_bounds__(NUM_THREADS, 1) k_gemm_grouped(const __grid_constant__ GroupedArgs g) {
-  // find this CTA's group by the prefix sums of the tile counts
-  int e = 0;
-  while (e + 1 < g.count && (int)blockIdx.x >= g.tile_start[e + 1]) ++e;
-  const int local = (int)blockIdx.x - g.tile_start[e];
-  const int tn = (g.N[e] + BN - 1) / BN;
-  TileJob j{&g.tmA[e], &g.tmB[e], g.sfa[e], g.sfb[e], g.ga[e], g.gb[e], g.d[e], (int64_t)g.N[e], g.M[e], g.N[e],
-            g.K[e], local / tn, local % tn};
-  gemm_tile(j, g.out_bf16 != 0, aligned_smem(), g.err);
+  GroupedSched s{&g};
+  gemm_persistent(s, g.out_bf16 != 0, g.err);
 }
 
 // ---------------------------------------------------------------------------
@@ -373,8 +532,33 @@ bool make_code_map(CUtensorMap* m, const uint8_t* codes, int64_t rows, int64_t K
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// D: rows x cols of bf16/fp32 with leading dimension ldd; box = 128 B x 32 rows, 128B swizzle
+bool make_out_map(CUtensorMap* m, void* d, int64_t rows, int64_t cols, int64_t ldd, bool bf16) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const int es = bf16 ? 2 : 4;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(ldd * es)};
+  cuuint32_t box[2] = {(cuuint32_t)(128 / es), 32};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, d, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool smem_configured(const void* fn) {
   return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) == cudaSuccess;
+}
+
+int num_sms() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
 }
 
 }  // namespace
@@ -393,8 +577,9 @@ int gemm_tile_n() { return BN; }
 
 cudaError_t launch_gemm(const GemmOperand& A, const GemmOperand& B, void* D, int64_t ldd, bool out_bf16, cudaStream_t s,
                         const char** why) {
-  CUtensorMap ta, tb;
-  if (!make_code_map(&ta, A.codes, A.rows, A.K, BM) || !make_code_map(&tb, B.codes, B.rows, B.K, BN)) {
+  CUtensorMap ta, tb, td;
+  if (!make_code_map(&ta, A.codes, A.rows, A.K, BM) || !make_code_map(&tb, B.codes, B.rows, B.K, BN) ||
+      !make_out_map(&td, D, A.rows, B.rows, ldd, out_bf16)) {
     *why = "cuTensorMapEncodeTiled failed (or driver entry point unavailable)";
     return cudaErrorInvalidValue;
   }
@@ -411,9 +596,10 @@ cudaError_t launch_gemm(const GemmOperand& A, const GemmOperand& B, void* D, int
     }
     cfg = true;
   }
-  GemmArgs a{A.scales, B.scales, A.g, B.g, D, ldd, (int)A.rows, (int)B.rows, (int)A.K, out_bf16 ? 1 : 0, err};
-  dim3 grid((unsigned)((B.rows + BN - 1) / BN), (unsigned)(A.rows / BM));
-  k_gemm<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(ta, tb, a);
+  GemmArgs a{A.scales, B.scales, A.g, B.g, (int)A.rows, (int)B.rows, (int)A.K, out_bf16 ? 1 : 0, err};
+  const int tiles = (int)(A.rows / BM) * (int)((B.rows + BN - 1) / BN);
+  const int grid = tiles < num_sms() ? tiles : num_sms();
+  k_gemm<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(ta, tb, td, a);
   return cudaGetLastError();
 }
 
@@ -442,7 +628,8 @@ cudaError_t launch_gemm_grouped(int count, const GemmOperand* A, const GemmOpera
     for (int e = 0; e < n; ++e) {
       const GemmOperand& a = A[base + e];
       const GemmOperand& b = B[base + e];
-      if (!make_code_map(&g.tmA[e], a.codes, a.rows, a.K, BM) || !make_code_map(&g.tmB[e], b.codes, b.rows, b.K, BN)) {
+      if (!make_code_map(&g.tmA[e], a.codes, a.rows, a.K, BM) || !make_code_map(&g.tmB[e], b.codes, b.rows, b.K, BN) ||
+          !make_out_map(&g.tmD[e], D[base + e], a.rows, b.rows, b.rows, out_bf16)) {
         *why = "cuTensorMapEncodeTiled failed (or driver entry point unavailable)";
         return cudaErrorInvalidValue;
       }
@@ -450,15 +637,16 @@ cudaError_t launch_gemm_grouped(int count, const GemmOperand* A, const GemmOpera
       g.sfb[e] = b.scales;
       g.ga[e] = a.g;
       g.gb[e] = b.g;
-      g.d[e] = D[base + e];
       g.M[e] = (int)a.rows;
       g.N[e] = (int)b.rows;
       g.K[e] = (int)a.K;
       g.tile_start[e] = tiles;
       tiles += (int)(a.rows / BM) * (int)((b.rows + BN - 1) / BN);
     }
+    g.tile_start[n] = tiles;
     if (tiles == 0) continue;
-    k_gemm_grouped<<<tiles, NUM_THREADS, SMEM_BYTES, s>>>(g);
+    const int grid = tiles < num_sms() ? tiles : num_sms();
+    k_gemm_grouped<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(g);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

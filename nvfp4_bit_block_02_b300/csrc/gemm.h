@@ -19,8 +19,6 @@ struct GemmArgs {
   const uint8_t* sfb;
   const float* ga;
   const float* gb;
-  void* d;
-  int64_t ldd;
   int M, N, K;
   int out_bf16;
   unsigned int* err;
@@ -31,13 +29,13 @@ constexpr int kGroupsPerLaunch = 64;
 struct GroupedArgs {
   CUtensorMap tmA[kGroupsPerLaunch];
   CUtensorMap tmB[kGroupsPerLaunch];
+  CUtensorMap tmD[kGroupsPerLaunch];
   const uint8_t* sfa[kGroupsPerLaunch];
   const uint8_t* sfb[kGroupsPerLaunch];
   const float* ga[kGroupsPerLaunch];
   const float* gb[kGroupsPerLaunch];
-  void* d[kGroupsPerLaunch];
   int M[kGroupsPerLaunch], N[kGroupsPerLaunch], K[kGroupsPerLaunch];
-  int tile_start[kGroupsPerLaunch];
+  int tile_start[kGroupsPerLaunch + 1];
   int count;
   int out_bf16;
   unsigned int* err;
