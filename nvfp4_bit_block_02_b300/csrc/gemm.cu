@@ -6,35 +6,36 @@
 // format of "NVIDIA Introduces a 4-Bit Pretraining Methodology Using NVFP4"
 // ("Summary").
 //
-// Persistent kernel, one CTA per SM, 128 x 256 output tiles in a grouped
-// raster order.  Warp roles (14 warps):
-//   warp 0       TMA producer: A and B code tiles (128 B of K = 256 elements
-//                per row, 128B swizzle) by cp.async.bulk.tensor and the
-//                matching 512-byte scale atoms by cp.async.bulk, into a
-//                3-stage shared-memory ring.
-//   warp 1       owns the tensor memory (512 columns: the 256-column FP32
-//                accumulator, then one scale slot per stage) and issues, from
-//                one thread, tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X
-//                (M = 128, N = 256, K = 64 per instruction).
-//   warps 2..5   scale warps: each owns one TMEM lane quarter and moves the
-//                stage's scale bytes from shared memory into the stage's scale
-//                slot with tcgen05.st.  For K-step j the MMA takes the 4 scales
-//                of row r from lane r % 32, column (scale address + r / 32), with
-//                scale address slot + 4j (A) and slot + 8j (B, 256 rows); lane l
-//                of quarter q holds the same words as lane l of quarter 0 (the
-//                layout tcgen05.cp .32x128b.warpx4 produces), so row l of each
-//                512-byte scale atom is one 16-byte load and four columns.  One
-//                16- (A) and one 32-column (B) store per warp and stage replace
-//                twelve tcgen05.cp, which occupied the tensor pipe longer than
-//                the MMAs themselves.
-//   warps 6..13  epilogue: two warps per lane quarter (128 columns each) drain
-//                the accumulator with tcgen05.ld, release it to the MMA warp,
-//                scale by g_A*g_B, convert, stage 32 x 128-byte boxes in
-//                swizzled shared memory and write them with TMA stores, while
-//                the next tile's mainloop runs.
+// Persistent kernel on CTA pairs (clusters of 2, one CTA per SM).  A pair
+// computes a 256 x 256 output tile with tcgen05.mma.cta_group::2 (M = 256,
+// N = 256, K = 64 per instruction, kind::mxf4nvf4.block_scale.scale_vec::4X):
+// CTA r of the pair holds rows 128r..128r+127 of the A tile and of the B tile
+// in its shared memory and rows 128r.. of the accumulator in its tensor
+// memory, so each SM loads a quarter of the tile's operand bytes.  Roles in
+// each CTA (15 warps):
+//   warp 0       TMA producer: its A and B halves (128 B of K = 256 elements
+//                per row, 128B swizzle; completion counted on the leader
+//                CTA's barrier) into a 5-stage ring.
+//   warp 14      scale producer: the stage's scale atoms by cp.async.bulk on a
+//                barrier of their own (issuing them from warp 0 as well slowed
+//                the operand stream by ~15%).
+//   warp 1       tensor memory owner (both CTAs allocate together); in the
+//                leader CTA one thread issues the pair's MMAs and commits to
+//                both CTAs' barriers.
+//   warps 2..5   scale warps: tcgen05.st of the stage's scale bytes into the
+//                CTA's tensor memory.  For K-step j the MMA reads the 4 scales
+//                of row r from lane r % 32, column (scale address + r / 32) of
+//                every lane quarter (the layout tcgen05.cp .32x128b.warpx4
+//                makes), scale address = slot + 4j (A), slot + 8j (B).
+//   warps 6..13  epilogue: two warps per lane quarter drain the CTA's 128 x 256
+//                accumulator half with tcgen05.ld, release it, scale by
+//                g_A*g_B, convert, and write 32 x 128-byte boxes through
+//                swizzled shared memory with TMA stores while the next tile's
+//                mainloop runs.
 // Every mbarrier wait is bounded (kWaitLimitNs).  On expiry the CTA records a
 // timeout in a device word, every role leaves its loop, in-flight copies and
-// MMAs are waited for (bounded), tensor memory is freed and the kernel returns.
+// MMAs are waited for (bounded), both CTAs meet at a final cluster barrier,
+// tensor memory is freed and the kernel returns.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -43,19 +44,28 @@
 
 #include "gemm.h"
 
+#ifndef NVFP4_SFB_MODE
+#define NVFP4_SFB_MODE 0  // 0: every CTA holds the scales of all 256 B rows
+#endif
+
 namespace nvfp4 {
 namespace {
 
-constexpr int BM = 128;
-constexpr int BN = 256;
-constexpr int BKB = 128;  // bytes of K per stage per row = 256 FP4 elements
-constexpr int STAGES = 3;
-constexpr int A_BYTES = BM * BKB;
-constexpr int B_BYTES = BN * BKB;
-constexpr int SFA_BYTES = 4 * 512;               // 4 K-atoms of the 128-row tile
-constexpr int SFB_BYTES = (BN / 128) * 4 * 512;  // per 128-row block of B
+constexpr int BM = 128;             // rows per CTA (the pair covers 256)
+constexpr int BN = 256;             // output columns per tile
+constexpr int BNH = BN / 2;         // B rows held by one CTA
+constexpr int BKB = 128;            // bytes of K per stage per row = 256 FP4 elements
+constexpr int STAGES = 5;
+constexpr int A_BYTES = BM * BKB;   // 16 KB
+constexpr int B_BYTES = BNH * BKB;  // 16 KB
+constexpr int SFA_BYTES = 4 * 512;  // 4 K-atoms of the CTA's 128 A rows
+#if NVFP4_SFB_MODE == 0
+constexpr int SFB_BYTES = 2 * 4 * 512;  // both 128-row blocks of B
+#else
+constexpr int SFB_BYTES = 4 * 512;
+#endif
 constexpr int EPI_WARPS = 8;
-constexpr int EPI_BYTES = 32 * 128;              // one 32-row x 128-byte box per epilogue warp
+constexpr int EPI_BYTES = 32 * 128;  // one 32-row x 128-byte box per epilogue warp
 constexpr int OFF_A = 0;
 constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
 constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
@@ -64,20 +74,20 @@ constexpr int OFF_EPI = OFF_SFB + STAGES * SFB_BYTES;
 constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * EPI_BYTES;
 constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;  // + barriers + alignment slack
 constexpr int TMEM_COLS = 512;
-constexpr int SFA_COL0 = BN;                    // scale slots: SFA 16 columns per stage,
-constexpr int SFB_COL0 = BN + 64;               //              SFB 32 columns per stage (32-aligned)
-constexpr int NUM_WARPS = 2 + 4 + EPI_WARPS;
+constexpr int SFA_COL0 = BN;                             // 16 columns per stage
+constexpr int SFB_COL0 = (SFA_COL0 + 16 * STAGES + 31) / 32 * 32;  // 32 columns per stage
+constexpr int NUM_WARPS = 2 + 4 + EPI_WARPS + 1;  // + the scale producer (last warp)
 constexpr int NUM_THREADS = 32 * NUM_WARPS;
-constexpr int GROUP_M = 16;                     // raster: 16 m-tiles per band
+constexpr int GROUP_M = 8;  // raster: bands of 8 pair rows
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
-static_assert(SFA_COL0 + 16 * STAGES <= SFB_COL0 && SFB_COL0 + 32 * STAGES <= TMEM_COLS, "TMEM budget");
+static_assert(SFB_COL0 + 32 * STAGES <= TMEM_COLS, "TMEM budget");
 static_assert(SFA_COL0 % 16 == 0 && SFB_COL0 % 32 == 0, "tcgen05.st .x16/.x32 need aligned columns");
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 static_assert(OFF_EPI % 1024 == 0 && OFF_B % 1024 == 0, "swizzled buffers need 1024-byte alignment");
 
 // instruction descriptor: E2M1 x E2M1 (kind::mxf4nvf4 encoding 1), UE4M3
-// scales, K-major A and B, dense K = 64, M and N fields.
-constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+// scales, K-major A and B, dense K = 64, N = 256, M = 256 (the pair).
+constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)((2 * BM) >> 4) << 24);
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -86,6 +96,30 @@ __device__ __forceinline__ unsigned long long now_ns() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_id() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t num_clusters() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// shared::cluster address of the same shared-memory offset in CTA `rank`
+__device__ __forceinline__ uint32_t peer_addr(uint32_t local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+  return r;
+}
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
@@ -93,14 +127,34 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+// arrive on a barrier given by its shared::cluster address (own or peer CTA).
+// Relaxed: what it publishes is tensor-memory state already completed by
+// tcgen05.wait::ld/st and ordered by tcgen05.fence::before_thread_sync; a
+// release at cluster scope would add a full memory fence on the scale path
+// of every K-step (measured: the pair kernel ran at half speed with it).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cbar) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cbar) : "memory");
 }
+// CTA-scope poll: every barrier here guards tensor-memory or async-proxy data
+// (TMA, tensor core), ordered by the tcgen05 fences around the waits, not
+// generic memory of the peer; a cluster-scope acquire cost ~130 cycles a poll.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// one non-blocking test of a phase
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
       : "r"(bar), "r"(parity)
@@ -133,10 +187,13 @@ __device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
   }
 }
 
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+// TMA load into this CTA's shared memory; completion is counted on the
+// barrier at shared::cluster address `cbar` (the leader CTA's, for the pair).
+__device__ __forceinline__ void tma_load_pair(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t cbar) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+      "[%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(cbar)
       : "memory");
 }
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
@@ -156,14 +213,20 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+// arrive (once, when this thread's MMAs complete) on the barrier at the same
+// offset in both CTAs of the pair
+__device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"((uint16_t)3)
+      : "memory");
 }
-__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t sfa, uint32_t sfb, uint32_t acc) {
+__device__ __forceinline__ void tc_mma_pair(uint32_t d, uint64_t a, uint64_t b, uint32_t sfa, uint32_t sfb,
+                                            uint32_t acc) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d),
+      "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d),
       "l"(a), "l"(b), "r"(kIdesc), "r"(acc), "r"(sfa), "r"(sfb)
       : "memory");
 }
@@ -210,7 +273,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&p);
 }
 
-// One output tile and the operands it reads.
+// One pair tile (256 x 256 outputs) and the operands it reads.
 struct Tile {
   const CUtensorMap* tmA;
   const CUtensorMap* tmB;
@@ -219,18 +282,18 @@ struct Tile {
   const uint8_t* sfb;
   const float* ga;
   const float* gb;
-  int N, K;
-  int m_tile, n_tile;
+  int M, N, K;
+  int pm, pn;  // pair-row (256-row) and column (256-col) tile indices
 };
 
-// Raster order: bands of GROUP_M m-tiles; inside a band n-tiles advance
-// slowest, so the CTAs working at one time share A and B rows in L2.
-__device__ __forceinline__ void raster(int t, int mt, int nt, int& m_tile, int& n_tile) {
+// Raster order: bands of GROUP_M pair rows; inside a band columns advance
+// slowest, so the pairs working at one time share A and B rows in L2.
+__device__ __forceinline__ void raster(int t, int mt, int nt, int& pm, int& pn) {
   const int band_tiles = GROUP_M * nt;
   const int band = t / band_tiles, in = t % band_tiles;
   const int rows = min(GROUP_M, mt - band * GROUP_M);
-  m_tile = band * GROUP_M + in % rows;
-  n_tile = in / rows;
+  pm = band * GROUP_M + in % rows;
+  pn = in / rows;
 }
 
 struct SingleSched {
@@ -238,10 +301,10 @@ struct SingleSched {
   const CUtensorMap* tmB;
   const CUtensorMap* tmD;
   const GemmArgs* a;
-  __device__ int num_tiles() const { return (a->M / BM) * ((a->N + BN - 1) / BN); }
+  __device__ int num_tiles() const { return ((a->M + 2 * BM - 1) / (2 * BM)) * ((a->N + BN - 1) / BN); }
   __device__ Tile get(int t) const {
-    Tile x{tmA, tmB, tmD, a->sfa, a->sfb, a->ga, a->gb, a->N, a->K, 0, 0};
-    raster(t, a->M / BM, (a->N + BN - 1) / BN, x.m_tile, x.n_tile);
+    Tile x{tmA, tmB, tmD, a->sfa, a->sfb, a->ga, a->gb, a->M, a->N, a->K, 0, 0};
+    raster(t, (a->M + 2 * BM - 1) / (2 * BM), (a->N + BN - 1) / BN, x.pm, x.pn);
     return x;
   }
 };
@@ -252,121 +315,140 @@ struct GroupedSched {
   __device__ Tile get(int t) const {
     int e = 0;
     while (e + 1 < g->count && t >= g->tile_start[e + 1]) ++e;
-    Tile x{&g->tmA[e], &g->tmB[e], &g->tmD[e], g->sfa[e], g->sfb[e], g->ga[e], g->gb[e], g->N[e], g->K[e], 0, 0};
-    raster(t - g->tile_start[e], g->M[e] / BM, (g->N[e] + BN - 1) / BN, x.m_tile, x.n_tile);
+    Tile x{&g->tmA[e], &g->tmB[e], &g->tmD[e], g->sfa[e], g->sfb[e], g->ga[e], g->gb[e], g->M[e], g->N[e], g->K[e], 0, 0};
+    raster(t - g->tile_start[e], (g->M[e] + 2 * BM - 1) / (2 * BM), (g->N[e] + BN - 1) / BN, x.pm, x.pn);
     return x;
   }
 };
 
 template <class Sched>
-__device__ __forceinline__ void gemm_persistent(const Sched& sched, bool out_bf16, unsigned int* err) {
+__device__ __forceinline__ void gemm_pairs(const Sched& sched, bool out_bf16, unsigned int* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
-  // barrier block: full[S], empty[S], sfready[S], accum_full, accum_empty, drain
-  const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * STAGES, sfr0 = empty0 + 8 * STAGES;
-  const uint32_t accum_full = sfr0 + 8 * STAGES, accum_empty = accum_full + 8, drain = accum_empty + 8;
+  // per CTA: full[S] (leader: A/B bytes of both CTAs + the 8 scale warps of
+  // the pair, so the MMA thread polls one barrier per stage), sf_full[S] (own
+  // scale bytes), empty[S], accum_full, accum_empty (leader: 16 epilogue
+  // warps), drain
+  const uint32_t full0 = smem_u32(bars), sff0 = full0 + 8 * STAGES, empty0 = sff0 + 8 * STAGES;
+  const uint32_t accum_full = empty0 + 8 * STAGES, accum_empty = accum_full + 8, drain = accum_empty + 8;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 3);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const bool leader = rank == 0;
   const int num_tiles = sched.num_tiles();
+  const int first = (int)cluster_id(), step = (int)num_clusters();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full0 + 8 * s, 1);
+      mbar_init(full0 + 8 * s, 1 + 8);
+      mbar_init(sff0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, 1);
-      mbar_init(sfr0 + 8 * s, 4);
     }
     mbar_init(accum_full, 1);
-    mbar_init(accum_empty, EPI_WARPS);
+    mbar_init(accum_empty, 2 * EPI_WARPS);
     mbar_init(drain, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
-  if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+  if (warp == 1) {  // both CTAs: the pair's tensor memory is allocated together
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                  "r"(TMEM_COLS));
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;");
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // both CTAs' barriers are initialised before any remote signal
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    // ---------------- TMA producer ----------------
+    // ---------------- TMA producer (each CTA: its halves) ----------------
     if (lane == 0) {
       uint32_t it = 0;
-      for (int t = blockIdx.x; t < num_tiles && !*abort_flag; t += gridDim.x) {
+      const uint32_t lead_full0 = peer_addr(full0, 0);
+      for (int t = first; t < num_tiles && !*abort_flag; t += step) {
         const Tile x = sched.get(t);
         const int nk = x.K / 256;
-        const int64_t nka = x.K / 64;
-        const int nb_valid = min(BN / 128, (x.N - x.n_tile * BN) / 128);
-        const uint32_t tx = A_BYTES + B_BYTES + SFA_BYTES + nb_valid * 2048;
+        const int m_tile = 2 * x.pm + (int)rank;               // this CTA's 128 A rows
+        const bool a_valid = m_tile * BM < x.M;
+        const int nb_mine = 2 * x.pn + (int)rank;              // this CTA's 128 B rows
+        const bool b_valid = nb_mine * 128 < x.N;
+        // the leader's halves always exist; the peer's may not (M or N % 256 == 128)
+        const uint32_t ab_tx = A_BYTES * (1 + ((2 * x.pm + 1) * BM < x.M)) + B_BYTES * (1 + ((2 * x.pn + 1) * 128 < x.N));
         for (int kt = 0; kt < nk; ++kt, ++it) {
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
           if (!mbar_wait(empty0 + 8 * s, ph ^ 1, abort_flag, err)) break;
-          const uint32_t fb = full0 + 8 * s;
-          mbar_expect_tx(fb, tx);
-          tma_load_2d(smem_u32(smem + OFF_A + s * A_BYTES), x.tmA, kt * BKB, x.m_tile * BM, fb);
-          tma_load_2d(smem_u32(smem + OFF_B + s * B_BYTES), x.tmB, kt * BKB, x.n_tile * BN, fb);
-          bulk_g2s(smem_u32(smem + OFF_SFA + s * SFA_BYTES), x.sfa + ((int64_t)x.m_tile * nka + 4 * kt) * 512,
-                   SFA_BYTES, fb);
-          for (int nb = 0; nb < nb_valid; ++nb)
-            bulk_g2s(smem_u32(smem + OFF_SFB + s * SFB_BYTES + nb * 2048),
-                     x.sfb + ((int64_t)(x.n_tile * (BN / 128) + nb) * nka + 4 * kt) * 512, 2048, fb);
+          // A/B: the leader expects both CTAs' bytes on its own barrier
+          if (leader) mbar_expect_tx(full0 + 8 * s, ab_tx);
+          const uint32_t fb = lead_full0 + 8 * s;
+          if (a_valid) tma_load_pair(smem_u32(smem + OFF_A + s * A_BYTES), x.tmA, kt * BKB, m_tile * BM, fb);
+          if (b_valid) tma_load_pair(smem_u32(smem + OFF_B + s * B_BYTES), x.tmB, kt * BKB, nb_mine * 128, fb);
         }
       }
-      if (*abort_flag) {  // let copies already issued land before the CTA exits
+      if (*abort_flag) {  // let copies already issued land before the CTA leaves
         const unsigned long long t0 = now_ns();
         while (now_ns() - t0 < 2000000ull) {
         }
       }
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer ----------------
-    if (lane == 0) {
-      uint32_t it = 0, ti = 0;
-      bool ok = true;
-      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++ti) {
+    // ---------------- MMA issuer (leader CTA) ----------------
+    if (leader && lane == 0) {
+      // the MMA issue queue is shallow, so every cycle spent between stages
+      // idles the tensor pipe: one barrier poll per stage, stage and phase kept
+      // incrementally, descriptors advanced by adding to their address field
+      // (K-step j is 32 bytes = 2 units further; a stage is A_BYTES / 16 units)
+      // The next stage's barrier is tested between the MMAs of the current
+      // one, while the tensor pipe is busy, so a ready stage costs no poll.
+      const uint64_t da0 = desc_sw128(smem_u32(smem + OFF_A)), db0 = desc_sw128(smem_u32(smem + OFF_B));
+      uint32_t s = 0, ph = 0, ti = 0;
+      bool ok = true, next_ready = false;
+      for (int t = first; t < num_tiles && ok; t += step, ++ti) {
         const Tile x = sched.get(t);
         const int nk = x.K / 256;
         if (!mbar_wait(accum_empty, (ti & 1) ^ 1, abort_flag, err)) break;
         tc_fence_after();
-        for (int kt = 0; kt < nk; ++kt, ++it) {
-          const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
-          if (!mbar_wait(sfr0 + 8 * s, ph, abort_flag, err) || !mbar_wait(full0 + 8 * s, ph, abort_flag, err)) {
+        for (int kt = 0; kt < nk; ++kt) {
+          if (!next_ready && !mbar_wait(full0 + 8 * s, ph, abort_flag, err)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = smem_u32(smem + OFF_A + s * A_BYTES);
-          const uint32_t b0 = smem_u32(smem + OFF_B + s * B_BYTES);
+          const uint32_t sn = s + 1 == STAGES ? 0 : s + 1, phn = s + 1 == STAGES ? ph ^ 1 : ph;
+          const uint64_t da = da0 + (uint64_t)(s * (A_BYTES >> 4)), db = db0 + (uint64_t)(s * (B_BYTES >> 4));
           const uint32_t sfa = tmem + SFA_COL0 + 16 * s, sfb = tmem + SFB_COL0 + 32 * s;
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            tc_mma(tmem, desc_sw128(a0 + 32 * j), desc_sw128(b0 + 32 * j), sfa + 4 * j, sfb + 8 * j, (kt | j) != 0);
-          tc_commit(empty0 + 8 * s);
+          for (int j = 0; j < 4; ++j) {
+            tc_mma_pair(tmem, da + 2 * j, db + 2 * j, sfa + 4 * j, sfb + 8 * j, (kt | j) != 0);
+            if (j == 2) next_ready = mbar_test(full0 + 8 * sn, phn);
+          }
+          tc_commit_pair(empty0 + 8 * s);
+          s = sn;
+          ph = phn;
         }
-        if (ok) tc_commit(accum_full);
+        next_ready = next_ready && ok;
+        if (ok) tc_commit_pair(accum_full);
       }
-      tc_commit(drain);  // arrives when every MMA this thread issued has completed
+      tc_commit_pair(drain);  // arrives when every MMA this thread issued has completed
       mbar_drain(drain, 0);
     }
   } else if (warp < 6) {
     // ---------------- scale warps: shared memory -> TMEM ----------------
     const uint32_t q = warp & 3;
     const uint32_t lane_base = (q * 32) << 16;
+    const uint32_t lead_full0 = peer_addr(full0, 0);
     uint32_t it = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+    for (int t = first; t < num_tiles && ok; t += step) {
       const Tile x = sched.get(t);
       const int nk = x.K / 256;
       for (int kt = 0; kt < nk; ++kt, ++it) {
         const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
         // warp vote: the tcgen05.st below is warp-collective
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(full0 + 8 * s, ph, abort_flag, err))) {
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(sff0 + 8 * s, ph, abort_flag, err))) {
           ok = false;
           break;
         }
@@ -376,10 +458,19 @@ __device__ __forceinline__ void gemm_persistent(const Sched& sched, bool out_bf1
         uint32_t va[16], vb[32];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const uint4 wa = sa[j * 32];           // A atom j
-          const uint4 w0 = sb[j * 32];           // B rows 0..127, atom j
-          const uint4 w1 = sb[128 + j * 32];     // B rows 128..255, atom j
+          const uint4 wa = sa[j * 32];
           va[4 * j] = wa.x; va[4 * j + 1] = wa.y; va[4 * j + 2] = wa.z; va[4 * j + 3] = wa.w;
+#if NVFP4_SFB_MODE == 0
+          const uint4 w0 = sb[j * 32];        // B rows 0..127 of the tile
+          const uint4 w1 = sb[128 + j * 32];  // B rows 128..255
+#elif NVFP4_SFB_MODE == 1
+          const uint4 w0 = sb[j * 32];        // own B rows at the first block position
+          const uint4 w1 = make_uint4(0, 0, 0, 0);
+#else
+          const uint4 own = sb[j * 32];       // own B rows at block position `rank`
+          const uint4 w0 = rank == 0 ? own : make_uint4(0, 0, 0, 0);
+          const uint4 w1 = rank == 0 ? make_uint4(0, 0, 0, 0) : own;
+#endif
           vb[8 * j] = w0.x; vb[8 * j + 1] = w0.y; vb[8 * j + 2] = w0.z; vb[8 * j + 3] = w0.w;
           vb[8 * j + 4] = w1.x; vb[8 * j + 5] = w1.y; vb[8 * j + 6] = w1.z; vb[8 * j + 7] = w1.w;
         }
@@ -388,43 +479,87 @@ __device__ __forceinline__ void gemm_persistent(const Sched& sched, bool out_bf1
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(sfr0 + 8 * s);
+        if (lane == 0) mbar_arrive_cluster(lead_full0 + 8 * s);
+      }
+    }
+  } else if (warp == NUM_WARPS - 1) {
+    // ---------------- scale producer (each CTA: its scale atoms) ----------------
+    if (lane == 0) {
+      uint32_t it = 0;
+      for (int t = first; t < num_tiles && !*abort_flag; t += step) {
+        const Tile x = sched.get(t);
+        const int nk = x.K / 256;
+        const int64_t nka = x.K / 64;
+        const int m_tile = 2 * x.pm + (int)rank;
+        const bool a_valid = m_tile * BM < x.M;
+#if NVFP4_SFB_MODE == 0
+        const int sfb_blocks = min(2, (x.N - x.pn * BN) / 128);
+        const int sfb_first = 2 * x.pn;
+#else
+        const int sfb_blocks = (2 * x.pn + (int)rank) * 128 < x.N ? 1 : 0;
+        const int sfb_first = 2 * x.pn + (int)rank;
+#endif
+        const uint32_t sf_tx = (a_valid ? SFA_BYTES : 0) + sfb_blocks * 2048;
+        for (int kt = 0; kt < nk; ++kt, ++it) {
+          const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
+          if (!mbar_wait(empty0 + 8 * s, ph ^ 1, abort_flag, err)) break;
+          const uint32_t sb = sff0 + 8 * s;
+          mbar_expect_tx(sb, sf_tx);
+          if (a_valid)
+            bulk_g2s(smem_u32(smem + OFF_SFA + s * SFA_BYTES), x.sfa + ((int64_t)m_tile * nka + 4 * kt) * 512,
+                     SFA_BYTES, sb);
+          for (int nb = 0; nb < sfb_blocks; ++nb)
+            bulk_g2s(smem_u32(smem + OFF_SFB + s * SFB_BYTES + nb * 2048),
+                     x.sfb + ((int64_t)(sfb_first + nb) * nka + 4 * kt) * 512, 2048, sb);
+        }
+      }
+      if (*abort_flag) {  // let copies already issued land before the CTA leaves
+        const unsigned long long t0 = now_ns();
+        while (now_ns() - t0 < 2000000ull) {
+        }
       }
     }
   } else {
-    // ---------------- epilogue ----------------
+    // ---------------- epilogue (each CTA: its 128 accumulator rows) ----------------
     const int e = warp - 6;
     const uint32_t q = warp & 3, half = e >> 2;
     const uint32_t taddr0 = tmem + ((q * 32) << 16) + half * 128;
     uint8_t* stage = smem + OFF_EPI + e * EPI_BYTES;
     const uint32_t stage_u32 = smem_u32(stage);
+    const uint32_t lead_accum_empty = peer_addr(accum_empty, 0);
     uint32_t ti = 0;
-    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++ti) {
+    for (int t = first; t < num_tiles; t += step, ++ti) {
       const Tile x = sched.get(t);
       // warp vote: tcgen05.ld is warp-collective
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(accum_full, ti & 1, abort_flag, err))) break;
       tc_fence_after();
       const float alpha = __fmul_rn(*x.ga, *x.gb);
-      const int col0 = x.n_tile * BN + half * 128;
-      const int row0 = x.m_tile * BM + q * 32;
-      const bool active = col0 < x.N;  // warp-uniform (N % 128 == 0)
+      const int col0 = x.pn * BN + half * 128;
+      const int row0 = (2 * x.pm + (int)rank) * BM + q * 32;
+      const bool active = col0 < x.N && row0 < x.M;  // warp-uniform (M, N % 128 == 0)
       if (out_bf16) {
         uint32_t pk[64];
         if (active) {
+          // two loads in flight per wait: the accumulator is released after two
+          // TMEM round trips instead of four
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t r[32];
-            NVFP4_LD32(taddr0 + c * 32, r);
+          for (int c = 0; c < 4; c += 2) {
+            uint32_t r0[32], r1[32];
+            NVFP4_LD32(taddr0 + c * 32, r0);
+            NVFP4_LD32(taddr0 + c * 32 + 32, r1);
             tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-              pk[16 * c + i] = pack_bf16(__fmul_rn(alpha, __uint_as_float(r[2 * i])),
-                                         __fmul_rn(alpha, __uint_as_float(r[2 * i + 1])));
+            for (int i = 0; i < 16; ++i) {
+              pk[16 * c + i] = pack_bf16(__fmul_rn(alpha, __uint_as_float(r0[2 * i])),
+                                         __fmul_rn(alpha, __uint_as_float(r0[2 * i + 1])));
+              pk[16 * c + 16 + i] = pack_bf16(__fmul_rn(alpha, __uint_as_float(r1[2 * i])),
+                                              __fmul_rn(alpha, __uint_as_float(r1[2 * i + 1])));
+            }
           }
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(accum_empty);
+        if (lane == 0) mbar_arrive_cluster(lead_accum_empty);
         if (active) {
 #pragma unroll
           for (int cc = 0; cc < 2; ++cc) {  // 64 columns = one 128-byte box row
@@ -453,7 +588,7 @@ __device__ __forceinline__ void gemm_persistent(const Sched& sched, bool out_bf1
           if (c == 3) {
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(accum_empty);
+            if (lane == 0) mbar_arrive_cluster(lead_accum_empty);
           }
           if (active) {
             if (lane == 0) bulk_wait_read0();
@@ -479,10 +614,11 @@ __device__ __forceinline__ void gemm_persistent(const Sched& sched, bool out_bf1
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // no CTA leaves while its peer may still signal it
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS));
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS));
   }
 }
 
@@ -490,12 +626,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
            const __grid_constant__ CUtensorMap tmD, const __grid_constant__ GemmArgs a) {
   SingleSched s{&tmA, &tmB, &tmD, &a};
-  gemm_persistent(s, a.out_bf16 != 0, a.err);
+  gemm_pairs(s, a.out_bf16 != 0, a.err);
 }
 
 __global__ void __launch_bounds__(NUM_THREADS, 1) k_gemm_grouped(const __grid_constant__ GroupedArgs g) {
   GroupedSched s{&g};
-  gemm_persistent(s, g.out_bf16 != 0, g.err);
+  gemm_pairs(s, g.out_bf16 != 0, g.err);
 }
 
 // ---------------------------------------------------------------------------
@@ -519,13 +655,13 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// rows x (K/2) bytes, K-major, box = 128 B x box_rows, 128B swizzle
-bool make_code_map(CUtensorMap* m, const uint8_t* codes, int64_t rows, int64_t K, int box_rows) {
+// rows x (K/2) bytes, K-major, box = 128 B x 128 rows, 128B swizzle
+bool make_code_map(CUtensorMap* m, const uint8_t* codes, int64_t rows, int64_t K) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)(K / 2), (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)(K / 2)};
-  cuuint32_t box[2] = {(cuuint32_t)BKB, (cuuint32_t)box_rows};
+  cuuint32_t box[2] = {(cuuint32_t)BKB, 128};
   cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(codes), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -561,6 +697,32 @@ int num_sms() {
   return n;
 }
 
+// grid of CTA pairs: one pair per two SMs, no more pairs than tiles
+template <class... Args>
+cudaError_t launch_pairs(void (*kernel)(Args...), int pair_tiles, int* max_pairs, cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (*max_pairs == 0) {  // pairs that can be resident at once (clusters live inside one GPC)
+    cfg.gridDim = dim3(2 * (unsigned)(num_sms() / 2), 1, 1);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(kernel), &cfg) != cudaSuccess || n <= 0)
+      n = num_sms() / 2;
+    *max_pairs = n;
+  }
+  const int pairs = pair_tiles < *max_pairs ? pair_tiles : *max_pairs;
+  cfg.gridDim = dim3((unsigned)(2 * (pairs > 0 ? pairs : 1)), 1, 1);
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 }  // namespace
 
 unsigned int* device_error_word() {
@@ -572,13 +734,13 @@ unsigned int* device_error_word() {
   return p;
 }
 
-int gemm_tile_m() { return BM; }
+int gemm_tile_m() { return 2 * BM; }
 int gemm_tile_n() { return BN; }
 
 cudaError_t launch_gemm(const GemmOperand& A, const GemmOperand& B, void* D, int64_t ldd, bool out_bf16, cudaStream_t s,
                         const char** why) {
   CUtensorMap ta, tb, td;
-  if (!make_code_map(&ta, A.codes, A.rows, A.K, BM) || !make_code_map(&tb, B.codes, B.rows, B.K, BN) ||
+  if (!make_code_map(&ta, A.codes, A.rows, A.K) || !make_code_map(&tb, B.codes, B.rows, B.K) ||
       !make_out_map(&td, D, A.rows, B.rows, ldd, out_bf16)) {
     *why = "cuTensorMapEncodeTiled failed (or driver entry point unavailable)";
     return cudaErrorInvalidValue;
@@ -591,16 +753,17 @@ cudaError_t launch_gemm(const GemmOperand& A, const GemmOperand& B, void* D, int
   static bool cfg = false;
   if (!cfg) {
     if (!smem_configured(reinterpret_cast<const void*>(k_gemm))) {
-      *why = "cudaFuncSetAttribute(max dynamic shared memory) failed";
+      *why = "cudaFuncSetAttribute failed";
       return cudaErrorInvalidValue;
     }
     cfg = true;
   }
   GemmArgs a{A.scales, B.scales, A.g, B.g, (int)A.rows, (int)B.rows, (int)A.K, out_bf16 ? 1 : 0, err};
-  const int tiles = (int)(A.rows / BM) * (int)((B.rows + BN - 1) / BN);
-  const int grid = tiles < num_sms() ? tiles : num_sms();
-  k_gemm<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(ta, tb, td, a);
-  return cudaGetLastError();
+  const int tiles = (int)((A.rows + 2 * BM - 1) / (2 * BM)) * (int)((B.rows + BN - 1) / BN);
+  static int max_pairs = 0;
+  cudaError_t e = launch_pairs(k_gemm, tiles, &max_pairs, s, ta, tb, td, a);
+  if (e != cudaSuccess) *why = "cudaLaunchKernelEx (cluster of 2) failed";
+  return e;
 }
 
 cudaError_t launch_gemm_grouped(int count, const GemmOperand* A, const GemmOperand* B, void* const* D, bool out_bf16,
@@ -613,7 +776,7 @@ cudaError_t launch_gemm_grouped(int count, const GemmOperand* A, const GemmOpera
   static bool cfg = false;
   if (!cfg) {
     if (!smem_configured(reinterpret_cast<const void*>(k_gemm_grouped))) {
-      *why = "cudaFuncSetAttribute(max dynamic shared memory) failed";
+      *why = "cudaFuncSetAttribute failed";
       return cudaErrorInvalidValue;
     }
     cfg = true;
@@ -628,7 +791,7 @@ cudaError_t launch_gemm_grouped(int count, const GemmOperand* A, const GemmOpera
     for (int e = 0; e < n; ++e) {
       const GemmOperand& a = A[base + e];
       const GemmOperand& b = B[base + e];
-      if (!make_code_map(&g.tmA[e], a.codes, a.rows, a.K, BM) || !make_code_map(&g.tmB[e], b.codes, b.rows, b.K, BN) ||
+      if (!make_code_map(&g.tmA[e], a.codes, a.rows, a.K) || !make_code_map(&g.tmB[e], b.codes, b.rows, b.K) ||
           !make_out_map(&g.tmD[e], D[base + e], a.rows, b.rows, b.rows, out_bf16)) {
         *why = "cuTensorMapEncodeTiled failed (or driver entry point unavailable)";
         return cudaErrorInvalidValue;
@@ -641,14 +804,16 @@ cudaError_t launch_gemm_grouped(int count, const GemmOperand* A, const GemmOpera
       g.N[e] = (int)b.rows;
       g.K[e] = (int)a.K;
       g.tile_start[e] = tiles;
-      tiles += (int)(a.rows / BM) * (int)((b.rows + BN - 1) / BN);
+      tiles += (int)((a.rows + 2 * BM - 1) / (2 * BM)) * (int)((b.rows + BN - 1) / BN);
     }
     g.tile_start[n] = tiles;
     if (tiles == 0) continue;
-    const int grid = tiles < num_sms() ? tiles : num_sms();
-    k_gemm_grouped<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(g);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    static int max_pairs = 0;
+    cudaError_t e = launch_pairs(k_gemm_grouped, tiles, &max_pairs, s, g);
+    if (e != cudaSuccess) {
+      *why = "cudaLaunchKernelEx (cluster of 2) failed";
+      return e;
+    }
   }
   return cudaSuccess;
 }
