@@ -57,18 +57,20 @@ __device__ __forceinline__ float e2m1_value(uint32_t code) {
 }
 
 // Stochastic rounding of q to a 4-bit code with a 16-bit uniform number:
-// neighbours lo <= |q| < hi on the grid, frac = (|q| - lo) / (hi - lo)
-// (exact), round up iff u16 < fl(frac * 65536); |q| >= 6 saturates.
+// neighbours lo <= |q| < hi on the grid, frac = (|q| - lo) / (hi - lo),
+// round up iff u16 < fl(frac * 65536); |q| >= 6 saturates.  The grid step of
+// |q|'s binade is 0.5, 1 or 2, so with t = |q| / step (exact) lo = floor(t) *
+// step and frac = t - floor(t), both exact: the same values as the division.
 __device__ __forceinline__ uint32_t e2m1_sr(float q, uint32_t u16) {
   uint32_t sign = (__float_as_uint(q) >> 28) & 8u;
   float a = fabsf(q);
   if (!(a < 6.0f)) return sign | 7u;
-  uint32_t lo = (a >= 0.5f) + (a >= 1.0f) + (a >= 1.5f) + (a >= 2.0f) + (a >= 3.0f) + (a >= 4.0f);
-  float flo = e2m1_mag(lo), fhi = e2m1_mag(lo + 1);
-  float frac = __fdiv_rn(__fsub_rn(a, flo), __fsub_rn(fhi, flo));
-  float thr = __fmul_rn(frac, 65536.0f);
-  uint32_t up = __uint2float_rn(u16) < thr;
-  return sign | (lo + up);
+  const float inv = a < 2.0f ? 2.0f : (a < 4.0f ? 1.0f : 0.5f);
+  const float t = __fmul_rn(a, inv);
+  const float fl = floorf(t);
+  const float thr = __fmul_rn(__fsub_rn(t, fl), 65536.0f);
+  const uint32_t lo = (uint32_t)fl + (a >= 2.0f ? 2u : 0u) + (a >= 4.0f ? 2u : 0u);
+  return sign | (lo + (__uint2float_rn(u16) < thr ? 1u : 0u));
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }

@@ -65,30 +65,51 @@ __global__ void __launch_bounds__(256) k_amax(const T* __restrict__ x, int64_t r
 }
 
 // ---------------------------------------------------------------------------
-// Shared encode step for one thread's two blocks.
+// Raw 16-element block loads (kept packed until used, so a thread can hold
+// the next tile's blocks in flight while it encodes the current one).
 // ---------------------------------------------------------------------------
 template <typename T>
-__device__ __forceinline__ void load16(const T* p, float v[16]);
+struct RawBlock;
 template <>
-__device__ __forceinline__ void load16<__nv_bfloat16>(const __nv_bfloat16* p, float v[16]) {
-  const uint4* q = reinterpret_cast<const uint4*>(p);
-  uint4 a = __ldg(q), b = __ldg(q + 1);
-  uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    v[2 * i] = bf16_lo(w[i]);
-    v[2 * i + 1] = bf16_hi(w[i]);
+struct RawBlock<__nv_bfloat16> {
+  uint4 w[2];
+  __device__ __forceinline__ void load(const void* p) {
+    const uint4* q = reinterpret_cast<const uint4*>(p);
+    w[0] = __ldg(q);
+    w[1] = __ldg(q + 1);
   }
-}
+  __device__ __forceinline__ void zero() { w[0] = w[1] = make_uint4(0, 0, 0, 0); }
+  __device__ __forceinline__ void unpack(float v[16]) const {
+    const uint32_t u[8] = {w[0].x, w[0].y, w[0].z, w[0].w, w[1].x, w[1].y, w[1].z, w[1].w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      v[2 * i] = bf16_lo(u[i]);
+      v[2 * i + 1] = bf16_hi(u[i]);
+    }
+  }
+};
 template <>
-__device__ __forceinline__ void load16<float>(const float* p, float v[16]) {
-  const float4* q = reinterpret_cast<const float4*>(p);
+struct RawBlock<float> {
+  uint4 w[4];
+  __device__ __forceinline__ void load(const void* p) {
+    const uint4* q = reinterpret_cast<const uint4*>(p);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    float4 f = __ldg(q + i);
-    v[4 * i] = f.x; v[4 * i + 1] = f.y; v[4 * i + 2] = f.z; v[4 * i + 3] = f.w;
+    for (int i = 0; i < 4; ++i) w[i] = __ldg(q + i);
   }
-}
+  __device__ __forceinline__ void zero() {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) w[i] = make_uint4(0, 0, 0, 0);
+  }
+  __device__ __forceinline__ void unpack(float v[16]) const {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[4 * i] = __uint_as_float(w[i].x);
+      v[4 * i + 1] = __uint_as_float(w[i].y);
+      v[4 * i + 2] = __uint_as_float(w[i].z);
+      v[4 * i + 3] = __uint_as_float(w[i].w);
+    }
+  }
+};
 
 __device__ __forceinline__ float absmax16(const float v[16]) {
   float m = 0.0f;
@@ -98,9 +119,11 @@ __device__ __forceinline__ float absmax16(const float v[16]) {
 }
 
 // ---------------------------------------------------------------------------
-// Row-wise encoder: K = cols.  Thread t of the 256 owns blocks
-// (row R0 + t/4 + 64h, block KB0 + t%4), h = 0, 1.  A 2D tile's 16 rows are the
-// 8-row groups of warps 2i and 2i+1 (lane bits 2..4 = row bits 0..2).
+// Row-wise encoder: K = cols.  Persistent: CTA b handles tiles b, b + G, ...
+// of 128 rows x 4 blocks; thread t owns blocks (row t/4 + 64h, block t%4) of
+// the tile, h = 0, 1, and loads the next tile's blocks before encoding the
+// current ones.  A 2D tile's 16 rows are the 8-row groups of warps 2i and
+// 2i+1 (lane bits 2..4 = row bits 0..2).
 // ---------------------------------------------------------------------------
 template <typename T, bool B2D, bool SR, bool F46, bool RHT, bool AMAX_ONLY>
 __global__ void __launch_bounds__(256) k_quant_rows(QuantArgs a) {
@@ -109,112 +132,134 @@ __global__ void __launch_bounds__(256) k_quant_rows(QuantArgs a) {
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const int kbl = t & 3, rl = t >> 2;
   const int64_t KB = a.K / 16, nka = (KB + 3) / 4;
-  const int64_t kb = (int64_t)blockIdx.x * 4 + kbl;
+  const int64_t tiles_x = nka, ntiles = tiles_x * ((a.R + 127) / 128);
   uint32_t mask = 0;
   if constexpr (RHT) mask = rht_sign_mask(a.rht_seed);
-
-  float v[2][16];
-  bool valid[2];
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    int64_t r = (int64_t)blockIdx.y * 128 + rl + 64 * h;
-    valid[h] = r < a.R && kb < KB;
-    if (valid[h]) {
-      load16<T>(reinterpret_cast<const T*>(a.x) + r * a.ld + kb * 16, v[h]);
-    } else {
-#pragma unroll
-      for (int i = 0; i < 16; ++i) v[h][i] = 0.0f;
-    }
-    if constexpr (RHT) rht16(v[h], mask);
-  }
-
-  if constexpr (AMAX_ONLY) {
-    uint32_t m = __float_as_uint(fmaxf(absmax16(v[0]), absmax16(v[1])));
-    cta_max_to_global(m, reinterpret_cast<unsigned int*>(a.amax_accum));
-    return;
-  } else {
-    const float amax = *a.amax_in;
-    const float g = global_scale(amax);
-    if (blockIdx.x == 0 && blockIdx.y == 0 && t == 0) {
+  float g = 1.0f, amax = 0.0f;
+  if constexpr (!AMAX_ONLY) {
+    amax = *a.amax_in;
+    g = global_scale(amax);
+    if (blockIdx.x == 0 && t == 0) {
       *a.g_out = g;
       if (a.amax_out != a.amax_in) *a.amax_out = amax;
     }
-    float ab[2] = {absmax16(v[0]), absmax16(v[1])};
-    if constexpr (B2D) {
+  }
+  const float g6 = __fmul_rn(6.0f, g), g4 = __fmul_rn(4.0f, g);
+  float run_max = 0.0f;
+
+  auto block_of = [&](int64_t tile, int h, int64_t& r, int64_t& kb) {
+    r = (tile / tiles_x) * 128 + rl + 64 * h;
+    kb = (tile % tiles_x) * 4 + kbl;
+  };
+  auto load = [&](int64_t tile, RawBlock<T> (&raw)[2]) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      int64_t r, kb;
+      block_of(tile, h, r, kb);
+      if (r < a.R && kb < KB) raw[h].load(reinterpret_cast<const T*>(a.x) + r * a.ld + kb * 16);
+      else raw[h].zero();
+    }
+  };
+
+  RawBlock<T> cur[2], nxt[2];
+  int64_t tile = blockIdx.x;
+  if (tile < ntiles) load(tile, cur);
+  for (; tile < ntiles; tile += gridDim.x) {
+    if (tile + gridDim.x < ntiles) load(tile + gridDim.x, nxt);
+    float v[2][16];
+    bool valid[2];
+    int64_t r[2], kb[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      block_of(tile, h, r[h], kb[h]);
+      valid[h] = r[h] < a.R && kb[h] < KB;
+      cur[h].unpack(v[h]);
+      if constexpr (RHT) rht16(v[h], mask);
+    }
+    if constexpr (AMAX_ONLY) {
+      run_max = fmaxf(run_max, fmaxf(absmax16(v[0]), absmax16(v[1])));
+    } else {
+      float ab[2] = {absmax16(v[0]), absmax16(v[1])};
+      if constexpr (B2D) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          float m = ab[h];
+          m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
+          m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 8));
+          m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 16));
+          if (lane < 4) xw[warp][h][kbl] = m;
+          ab[h] = m;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int h = 0; h < 2; ++h) ab[h] = fmaxf(ab[h], xw[warp ^ 1][h][kbl]);
+      }
+      uint2 codes[2];
+      uint32_t sbyte[2];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        float m = ab[h];
-        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
-        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 8));
-        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 16));
-        if (lane < 4) xw[warp][h][kbl] = m;
-        ab[h] = m;
-      }
-      __syncthreads();
+        uint32_t u[16];
+        if constexpr (SR) sr_draws16(a.seed, a.offset, (uint64_t)(r[h] * a.K + kb[h] * 16), u);
+        float s6, r6;
+        sbyte[h] = block_scale(ab[h], g6, g, s6, r6);
+        codes[h] = encode16<SR>(v[h], r6, u);
+        if constexpr (F46) {
+          float s4, r4;
+          uint32_t b4 = block_scale(ab[h], g4, g, s4, r4);
+          uint2 c4 = encode16<SR>(v[h], r4, u);
+          float e6 = block_sq_err16(v[h], codes[h], s6, g);
+          float e4 = block_sq_err16(v[h], c4, s4, g);
+          if constexpr (B2D) {
 #pragma unroll
-      for (int h = 0; h < 2; ++h) ab[h] = fmaxf(ab[h], xw[warp ^ 1][h][kbl]);
-    }
-    const float g6 = __fmul_rn(6.0f, g), g4 = __fmul_rn(4.0f, g);
-    uint2 codes[2];
-    uint32_t sbyte[2];
-    uint32_t u[2][16];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      int64_t r = (int64_t)blockIdx.y * 128 + rl + 64 * h;
-      if constexpr (SR) sr_draws16(a.seed, a.offset, (uint64_t)(r * a.K + kb * 16), u[h]);
-      float s6, r6;
-      sbyte[h] = block_scale(ab[h], g6, g, s6, r6);
-      codes[h] = encode16<SR>(v[h], r6, u[h]);
-      if constexpr (F46) {
-        float s4, r4;
-        uint32_t b4 = block_scale(ab[h], g4, g, s4, r4);
-        uint2 c4 = encode16<SR>(v[h], r4, u[h]);
-        float e6 = block_sq_err16(v[h], codes[h], s6, g);
-        float e4 = block_sq_err16(v[h], c4, s4, g);
-        if constexpr (B2D) {
-#pragma unroll
-          for (int o = 4; o <= 16; o <<= 1) {
-            e6 = __fadd_rn(e6, __shfl_xor_sync(0xFFFFFFFFu, e6, o));
-            e4 = __fadd_rn(e4, __shfl_xor_sync(0xFFFFFFFFu, e4, o));
+            for (int o = 4; o <= 16; o <<= 1) {
+              e6 = __fadd_rn(e6, __shfl_xor_sync(0xFFFFFFFFu, e6, o));
+              e4 = __fadd_rn(e4, __shfl_xor_sync(0xFFFFFFFFu, e4, o));
+            }
+            __syncthreads();  // xw reuse: every thread has read the previous exchange
+            if (lane < 4) {
+              xw[warp][h][kbl] = e6;
+              xw4[warp][h][kbl] = e4;
+            }
+            __syncthreads();
+            // tile sum = rows 0..7 + rows 8..15 (fp add commutes)
+            e6 = __fadd_rn(e6, xw[warp ^ 1][h][kbl]);
+            e4 = __fadd_rn(e4, xw4[warp ^ 1][h][kbl]);
           }
-          __syncthreads();  // xw reuse: every thread has read the amax exchange
-          if (lane < 4) {
-            xw[warp][h][kbl] = e6;
-            xw4[warp][h][kbl] = e4;
+          if (e4 < e6) {
+            codes[h] = c4;
+            sbyte[h] = b4;
           }
-          __syncthreads();
-          // tile sum = rows 0..7 + rows 8..15 (lower warp first; fp add commutes)
-          e6 = __fadd_rn(e6, xw[warp ^ 1][h][kbl]);
-          e4 = __fadd_rn(e4, xw4[warp ^ 1][h][kbl]);
-        }
-        if (e4 < e6) {
-          codes[h] = c4;
-          sbyte[h] = b4;
         }
       }
-    }
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      int64_t r = (int64_t)blockIdx.y * 128 + rl + 64 * h;
-      if (valid[h]) {
-        *reinterpret_cast<uint2*>(a.codes + r * (a.K / 2) + kb * 8) = codes[h];
-        if (a.tdebug) {
-          float4* d = reinterpret_cast<float4*>(a.tdebug + r * a.K + kb * 16);
+      for (int h = 0; h < 2; ++h) {
+        if (valid[h]) {
+          *reinterpret_cast<uint2*>(a.codes + r[h] * (a.K / 2) + kb[h] * 8) = codes[h];
+          if (a.tdebug) {
+            float4* d = reinterpret_cast<float4*>(a.tdebug + r[h] * a.K + kb[h] * 16);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) d[i] = make_float4(v[h][4 * i], v[h][4 * i + 1], v[h][4 * i + 2], v[h][4 * i + 3]);
+            for (int i = 0; i < 4; ++i)
+              d[i] = make_float4(v[h][4 * i], v[h][4 * i + 1], v[h][4 * i + 2], v[h][4 * i + 3]);
+          }
         }
+        a.scales[sf_offset(r[h], kb[h], nka)] = valid[h] ? (uint8_t)sbyte[h] : (uint8_t)0;
       }
-      a.scales[sf_offset(r, kb, nka)] = valid[h] ? (uint8_t)sbyte[h] : (uint8_t)0;
+      if constexpr (B2D) __syncthreads();  // the exchange buffers are reused by the next tile
     }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) cur[h] = nxt[h];
   }
+  if constexpr (AMAX_ONLY) cta_max_to_global(__float_as_uint(run_max), reinterpret_cast<unsigned int*>(a.amax_accum));
 }
 
 // ---------------------------------------------------------------------------
 // Transposed encoder: x is [Tt][N] row-major, the output orientation is
-// N x Tt (K = Tt).  A CTA stages 64 input rows x 128 columns in shared memory;
-// thread t then owns output rows n0 + 2*(t%64) + {0, 1} and block t/64 of the
-// tile (16 consecutive input rows).  A 2D tile (16 output rows) is 8
-// consecutive lanes (lane bits 0..2 = row-pair bits).
+// N x Tt (K = Tt).  Persistent over tiles of 64 input rows x 128 columns: the
+// tile is staged in shared memory and read back as column pairs; thread t
+// then owns output rows n0 + 2*(t%64) + {0, 1} and block t/64 of the tile.  The
+// next tile's global loads are issued before the current tile is encoded.  A
+// 2D tile (16 output rows) is 8 consecutive lanes (lane bits 0..2 = row-pair
+// bits).
 // ---------------------------------------------------------------------------
 template <typename T>
 struct ColTile;
@@ -240,113 +285,132 @@ struct ColTile<float> {
 template <typename T, bool B2D, bool SR, bool F46, bool RHT, bool AMAX_ONLY>
 __global__ void __launch_bounds__(256) k_quant_cols(QuantArgs a) {
   constexpr int RB = ColTile<T>::kRowBytes;
-  __shared__ __align__(16) uint8_t tile[64 * RB];
-  const int t = threadIdx.x, lane = t & 31;
+  constexpr int VPR = RB / 16;                  // 16-byte vectors per tile row
+  constexpr int NV = (64 * VPR) / 256;          // vectors per thread
+  __shared__ __align__(16) uint8_t tile_s[64 * RB];
+  const int t = threadIdx.x;
   const int64_t Tt = a.R_in, N = a.C_in;  // input rows / cols
   const int64_t K = Tt, KB = K / 16, nka = (KB + 3) / 4;
-  const int64_t tok0 = (int64_t)blockIdx.y * 64, n0 = (int64_t)blockIdx.x * 128;
-
-  // stage the input tile (rows beyond Tt or columns beyond N read as zero)
-  constexpr int VPR = RB / 16;  // 16-byte vectors per tile row
-#pragma unroll
-  for (int i = 0; i < (64 * VPR) / 256; ++i) {
-    int idx = t + 256 * i, row = idx / VPR, cv = idx % VPR;
-    int64_t col = n0 + (int64_t)cv * (16 / sizeof(T));
-    uint4 w = make_uint4(0, 0, 0, 0);
-    if (tok0 + row < Tt && col < N)
-      w = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(a.x) + (tok0 + row) * a.ld + col));
-    *reinterpret_cast<uint4*>(tile + row * RB + cv * 16) = w;
-  }
-  __syncthreads();
-
+  const int64_t tiles_x = (N + 127) / 128, ntiles = tiles_x * ((Tt + 63) / 64);
   const int np = t & 63, kbl = t >> 6;
-  const int64_t kb = (int64_t)blockIdx.y * 4 + kbl;
   uint32_t mask = 0;
   if constexpr (RHT) mask = rht_sign_mask(a.rht_seed);
-  float v[2][16];
-#pragma unroll
-  for (int e = 0; e < 16; ++e) ColTile<T>::pair(tile, 16 * kbl + e, np, v[0][e], v[1][e]);
-  if constexpr (RHT) {
-    rht16(v[0], mask);
-    rht16(v[1], mask);
-  }
-  bool valid[2];
-#pragma unroll
-  for (int h = 0; h < 2; ++h) valid[h] = (n0 + 2 * np + h < N) && kb < KB;
-
-  if constexpr (AMAX_ONLY) {
-    uint32_t m = __float_as_uint(fmaxf(absmax16(v[0]), absmax16(v[1])));
-    cta_max_to_global(m, reinterpret_cast<unsigned int*>(a.amax_accum));
-    return;
-  } else {
+  float g = 1.0f;
+  if constexpr (!AMAX_ONLY) {
     const float amax = *a.amax_in;
-    const float g = global_scale(amax);
-    if (blockIdx.x == 0 && blockIdx.y == 0 && t == 0) {
+    g = global_scale(amax);
+    if (blockIdx.x == 0 && t == 0) {
       *a.g_out = g;
       if (a.amax_out != a.amax_in) *a.amax_out = amax;
     }
-    float ab[2] = {absmax16(v[0]), absmax16(v[1])};
-    if constexpr (B2D) {
-      float m = fmaxf(ab[0], ab[1]);
-      m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-      m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
-      m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
-      ab[0] = ab[1] = m;
-    }
-    const float g6 = __fmul_rn(6.0f, g), g4 = __fmul_rn(4.0f, g);
-    uint2 codes[2], c4[2];
-    uint32_t sbyte[2], b4[2];
-    float e6[2], e4[2];
-    uint32_t u[2][16];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      int64_t n = n0 + 2 * np + h;
-      if constexpr (SR) sr_draws16(a.seed, a.offset, (uint64_t)(n * K + kb * 16), u[h]);
-      float s6, r6;
-      sbyte[h] = block_scale(ab[h], g6, g, s6, r6);
-      codes[h] = encode16<SR>(v[h], r6, u[h]);
-      if constexpr (F46) {
-        float s4, r4;
-        b4[h] = block_scale(ab[h], g4, g, s4, r4);
-        c4[h] = encode16<SR>(v[h], r4, u[h]);
-        e6[h] = block_sq_err16(v[h], codes[h], s6, g);
-        e4[h] = block_sq_err16(v[h], c4[h], s4, g);
-      }
-    }
-    if constexpr (F46) {
-      if constexpr (B2D) {
-        // tile rows 2p, 2p+1 are this thread's pair; then pairs of pairs ...
-        float s6 = __fadd_rn(e6[0], e6[1]), s4 = __fadd_rn(e4[0], e4[1]);
-#pragma unroll
-        for (int o = 1; o <= 4; o <<= 1) {
-          s6 = __fadd_rn(s6, __shfl_xor_sync(0xFFFFFFFFu, s6, o));
-          s4 = __fadd_rn(s4, __shfl_xor_sync(0xFFFFFFFFu, s4, o));
-        }
-        e6[0] = e6[1] = s6;
-        e4[0] = e4[1] = s4;
-      }
-#pragma unroll
-      for (int h = 0; h < 2; ++h)
-        if (e4[h] < e6[h]) {
-          codes[h] = c4[h];
-          sbyte[h] = b4[h];
-        }
-    }
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      int64_t n = n0 + 2 * np + h;
-      if (valid[h]) {
-        *reinterpret_cast<uint2*>(a.codes + n * (K / 2) + kb * 8) = codes[h];
-        if (a.tdebug) {
-          float4* d = reinterpret_cast<float4*>(a.tdebug + n * K + kb * 16);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) d[i] = make_float4(v[h][4 * i], v[h][4 * i + 1], v[h][4 * i + 2], v[h][4 * i + 3]);
-        }
-      }
-      a.scales[sf_offset(n, kb, nka)] = valid[h] ? (uint8_t)sbyte[h] : (uint8_t)0;
-    }
-    (void)lane;
   }
+  const float g6 = __fmul_rn(6.0f, g), g4 = __fmul_rn(4.0f, g);
+  float run_max = 0.0f;
+
+  auto load = [&](int64_t tile, uint4 (&raw)[NV]) {
+    const int64_t tok0 = (tile / tiles_x) * 64, n0 = (tile % tiles_x) * 128;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      int idx = t + 256 * i, row = idx / VPR, cv = idx % VPR;
+      int64_t col = n0 + (int64_t)cv * (16 / sizeof(T));
+      raw[i] = make_uint4(0, 0, 0, 0);
+      if (tok0 + row < Tt && col < N)
+        raw[i] = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(a.x) + (tok0 + row) * a.ld + col));
+    }
+  };
+
+  uint4 raw[NV];
+  int64_t tile = blockIdx.x;
+  if (tile < ntiles) load(tile, raw);
+  for (; tile < ntiles; tile += gridDim.x) {
+    __syncthreads();  // the previous tile's readers are done with tile_s
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      int idx = t + 256 * i, row = idx / VPR, cv = idx % VPR;
+      *reinterpret_cast<uint4*>(tile_s + row * RB + cv * 16) = raw[i];
+    }
+    __syncthreads();
+    if (tile + gridDim.x < ntiles) load(tile + gridDim.x, raw);  // in flight during the encode
+
+    const int64_t n0 = (tile % tiles_x) * 128;
+    const int64_t kb = (tile / tiles_x) * 4 + kbl;
+    float v[2][16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) ColTile<T>::pair(tile_s, 16 * kbl + e, np, v[0][e], v[1][e]);
+    if constexpr (RHT) {
+      rht16(v[0], mask);
+      rht16(v[1], mask);
+    }
+    bool valid[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) valid[h] = (n0 + 2 * np + h < N) && kb < KB;
+
+    if constexpr (AMAX_ONLY) {
+      run_max = fmaxf(run_max, fmaxf(absmax16(v[0]), absmax16(v[1])));
+    } else {
+      float ab[2] = {absmax16(v[0]), absmax16(v[1])};
+      if constexpr (B2D) {
+        float m = fmaxf(ab[0], ab[1]);
+        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
+        ab[0] = ab[1] = m;
+      }
+      uint2 codes[2], c4[2];
+      uint32_t sbyte[2], b4[2];
+      float e6[2], e4[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int64_t n = n0 + 2 * np + h;
+        uint32_t u[16];
+        if constexpr (SR) sr_draws16(a.seed, a.offset, (uint64_t)(n * K + kb * 16), u);
+        float s6, r6;
+        sbyte[h] = block_scale(ab[h], g6, g, s6, r6);
+        codes[h] = encode16<SR>(v[h], r6, u);
+        if constexpr (F46) {
+          float s4, r4;
+          b4[h] = block_scale(ab[h], g4, g, s4, r4);
+          c4[h] = encode16<SR>(v[h], r4, u);
+          e6[h] = block_sq_err16(v[h], codes[h], s6, g);
+          e4[h] = block_sq_err16(v[h], c4[h], s4, g);
+        }
+      }
+      if constexpr (F46) {
+        if constexpr (B2D) {
+          // tile rows 2p, 2p+1 are this thread's pair; then pairs of pairs ...
+          float s6 = __fadd_rn(e6[0], e6[1]), s4 = __fadd_rn(e4[0], e4[1]);
+#pragma unroll
+          for (int o = 1; o <= 4; o <<= 1) {
+            s6 = __fadd_rn(s6, __shfl_xor_sync(0xFFFFFFFFu, s6, o));
+            s4 = __fadd_rn(s4, __shfl_xor_sync(0xFFFFFFFFu, s4, o));
+          }
+          e6[0] = e6[1] = s6;
+          e4[0] = e4[1] = s4;
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          if (e4[h] < e6[h]) {
+            codes[h] = c4[h];
+            sbyte[h] = b4[h];
+          }
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int64_t n = n0 + 2 * np + h;
+        if (valid[h]) {
+          *reinterpret_cast<uint2*>(a.codes + n * (K / 2) + kb * 8) = codes[h];
+          if (a.tdebug) {
+            float4* d = reinterpret_cast<float4*>(a.tdebug + n * K + kb * 16);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              d[i] = make_float4(v[h][4 * i], v[h][4 * i + 1], v[h][4 * i + 2], v[h][4 * i + 3]);
+          }
+        }
+        a.scales[sf_offset(n, kb, nka)] = valid[h] ? (uint8_t)sbyte[h] : (uint8_t)0;
+      }
+    }
+  }
+  if constexpr (AMAX_ONLY) cta_max_to_global(__float_as_uint(run_max), reinterpret_cast<unsigned int*>(a.amax_accum));
 }
 
 // ---------------------------------------------------------------------------
@@ -430,14 +494,30 @@ cudaError_t launch_amax(const void* x, bool bf16, int64_t rows, int64_t cols, in
   return cudaGetLastError();
 }
 
+// Persistent grids: as many CTAs as fit on the GPU at once (occupancy of the
+// instantiation), never more than there are tiles.
+template <class K>
+static unsigned persistent_grid(K kernel, int64_t tiles) {
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 256, 0) != cudaSuccess || per_sm <= 0) per_sm = 2;
+  const int64_t cap = (int64_t)num_sms() * per_sm;
+  return (unsigned)(tiles < cap ? (tiles > 0 ? tiles : 1) : cap);
+}
+
 template <typename T, bool B2D, bool SR, bool F46, bool RHT, bool AO>
 static void launch_q(const QuantArgs& a, bool transpose, cudaStream_t s) {
   if (!transpose) {
-    dim3 grid((unsigned)((a.K / 16 + 3) / 4), (unsigned)((a.R + 127) / 128));
-    k_quant_rows<T, B2D, SR, F46, RHT, AO><<<grid, 256, 0, s>>>(a);
+    const int64_t tiles = ((a.K / 16 + 3) / 4) * ((a.R + 127) / 128);
+    auto k = k_quant_rows<T, B2D, SR, F46, RHT, AO>;
+    static unsigned cap = 0;
+    if (!cap) cap = persistent_grid(k, (int64_t)1 << 40);
+    k<<<(unsigned)(tiles < cap ? tiles : cap), 256, 0, s>>>(a);
   } else {
-    dim3 grid((unsigned)((a.C_in + 127) / 128), (unsigned)((a.R_in + 63) / 64));
-    k_quant_cols<T, B2D, SR, F46, RHT, AO><<<grid, 256, 0, s>>>(a);
+    const int64_t tiles = ((a.C_in + 127) / 128) * ((a.R_in + 63) / 64);
+    auto k = k_quant_cols<T, B2D, SR, F46, RHT, AO>;
+    static unsigned cap = 0;
+    if (!cap) cap = persistent_grid(k, (int64_t)1 << 40);
+    k<<<(unsigned)(tiles < cap ? tiles : cap), 256, 0, s>>>(a);
   }
 }
 
