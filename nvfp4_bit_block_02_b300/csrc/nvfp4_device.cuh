@@ -1,8 +1,9 @@
 // Device helpers of the NVFP4 kernels (sm_103a).  Every fp32 operation that
-// decides a code or a scale is an explicit IEEE round-to-nearest intrinsic
-// (__fmul_rn, __fdiv_rn, __frcp_rn, __fadd_rn, __fsub_rn) so that the
-// compiler cannot contract or reorder it; the encoder's results are therefore
-// fixed bit for bit by the sequence written in nvfp4.h.
+// decides a code or a scale is an explicit IEEE intrinsic (__fmul_rn,
+// __fmul2_rn, __fdiv_rn, __frcp_rn, __fadd_rn, __fsub_rn, and one __fmaf_ru
+// whose exact result is rounded upward on purpose) so that the compiler
+// cannot contract or reorder it; the encoder's results are therefore fixed
+// bit for bit by the sequence written in nvfp4.h.
 #pragma once
 #include <cstdint>
 #include <cuda_bf16.h>
@@ -59,18 +60,24 @@ __device__ __forceinline__ float e2m1_value(uint32_t code) {
 // Stochastic rounding of q to a 4-bit code with a 16-bit uniform number:
 // neighbours lo <= |q| < hi on the grid, frac = (|q| - lo) / (hi - lo),
 // round up iff u16 < fl(frac * 65536); |q| >= 6 saturates.  The grid step of
-// |q|'s binade is 0.5, 1 or 2, so with t = |q| / step (exact) lo = floor(t) *
-// step and frac = t - floor(t), both exact: the same values as the division.
+// |q|'s binade is 0.5, 1 or 2, so with t = |q| / step (exact), lo = floor(t)
+// steps and frac * 65536 = T - 65536 * floor(t), T = t * 65536 (exact).  For an
+// integer u16, u16 < frac * 65536 iff ceil(T) + 65535 - u16 reaches the next
+// multiple of 65536, so the code index is (ceil(T) + (u16 ^ 0xFFFF)) >> 16 plus
+// the binade's first index.  ceil(T) comes from one fma rounded upward onto
+// the integer grid of [2^23, 2^24): every step is exact integer or IEEE
+// arithmetic, no conversion or floor instruction is needed, and |q| >= 6
+// (and any larger value, up to infinity) lands on index 7 through the min.
 __device__ __forceinline__ uint32_t e2m1_sr(float q, uint32_t u16) {
-  uint32_t sign = (__float_as_uint(q) >> 28) & 8u;
-  float a = fabsf(q);
-  if (!(a < 6.0f)) return sign | 7u;
-  const float inv = a < 2.0f ? 2.0f : (a < 4.0f ? 1.0f : 0.5f);
-  const float t = __fmul_rn(a, inv);
-  const float fl = floorf(t);
-  const float thr = __fmul_rn(__fsub_rn(t, fl), 65536.0f);
-  const uint32_t lo = (uint32_t)fl + (a >= 2.0f ? 2u : 0u) + (a >= 4.0f ? 2u : 0u);
-  return sign | (lo + (__uint2float_rn(u16) < thr ? 1u : 0u));
+  const uint32_t sign = (__float_as_uint(q) >> 28) & 8u;
+  const float a = fabsf(q);
+  const bool lt2 = a < 2.0f, lt4 = a < 4.0f;
+  const float k = lt2 ? 131072.0f : (lt4 ? 65536.0f : 32768.0f);  // 65536 / step
+  // 2^23's bit pattern is removed and the binade's first index (0, 2, 4) added
+  const uint32_t bias = lt2 ? 0xB5000000u : (lt4 ? 0xB5020000u : 0xB5040000u);
+  const float c = __fmaf_ru(a, k, 8388608.0f);  // 2^23 + ceil(T)
+  const uint32_t idx = (__float_as_uint(c) + (u16 ^ 0xFFFFu) + bias) >> 16;
+  return sign | min(idx, 7u);
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -160,11 +167,18 @@ __device__ __forceinline__ uint32_t block_scale(float amax_b, float mg, float g,
 }
 
 // Encode 16 values with block reciprocal rcp into two 32-bit words of codes.
+// The products are paired into packed fp32x2 multiplies (each lane an IEEE
+// round-to-nearest product, the same value as a scalar multiply).
 template <bool SR>
 __device__ __forceinline__ uint2 encode16(const float v[16], float rcp, const uint32_t* u) {
   float q[16];
+  const float2 rr = make_float2(rcp, rcp);
 #pragma unroll
-  for (int i = 0; i < 16; ++i) q[i] = __fmul_rn(v[i], rcp);
+  for (int i = 0; i < 8; ++i) {
+    const float2 p = __fmul2_rn(make_float2(v[2 * i], v[2 * i + 1]), rr);
+    q[2 * i] = p.x;
+    q[2 * i + 1] = p.y;
+  }
   if constexpr (!SR) {
     return make_uint2(e2m1x8_rne(q), e2m1x8_rne(q + 8));
   } else {

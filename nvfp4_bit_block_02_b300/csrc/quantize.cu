@@ -119,20 +119,44 @@ __device__ __forceinline__ float absmax16(const float v[16]) {
 }
 
 // ---------------------------------------------------------------------------
+// Persistent tile walk: tile t of a tiles_y x tiles_x grid is (t / tiles_x,
+// t % tiles_x); a CTA visits blockIdx.x, blockIdx.x + G, ... by adding
+// (G / tiles_x, G % tiles_x) with one carry, so the loop divides nothing.
+// ---------------------------------------------------------------------------
+struct TileWalk {
+  uint32_t tiles_x, dy, dx;
+  __device__ TileWalk(uint32_t tx) : tiles_x(tx), dy(gridDim.x / tx), dx(gridDim.x % tx) {}
+  __device__ void start(uint32_t& y, uint32_t& x) const {
+    y = blockIdx.x / tiles_x;
+    x = blockIdx.x % tiles_x;
+  }
+  __device__ void next(uint32_t y, uint32_t x, uint32_t& ny, uint32_t& nx) const {
+    nx = x + dx;
+    ny = y + dy;
+    if (nx >= tiles_x) {
+      nx -= tiles_x;
+      ++ny;
+    }
+  }
+};
+
+// ---------------------------------------------------------------------------
 // Row-wise encoder: K = cols.  Persistent: CTA b handles tiles b, b + G, ...
 // of 128 rows x 4 blocks; thread t owns blocks (row t/4 + 64h, block t%4) of
 // the tile, h = 0, 1, and loads the next tile's blocks before encoding the
 // current ones.  A 2D tile's 16 rows are the 8-row groups of warps 2i and
-// 2i+1 (lane bits 2..4 = row bits 0..2).
+// 2i+1 (lane bits 2..4 = row bits 0..2).  Index arithmetic is 32-bit (rows
+// and 16-element blocks each fit in 31 bits); byte offsets are 64-bit.
 // ---------------------------------------------------------------------------
 template <typename T, bool B2D, bool SR, bool F46, bool RHT, bool AMAX_ONLY>
 __global__ void __launch_bounds__(256) k_quant_rows(QuantArgs a) {
   __shared__ float xw[8][2][4];    // cross-warp exchange for 2D tiles
   __shared__ float xw4[8][2][4];
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  const int kbl = t & 3, rl = t >> 2;
-  const int64_t KB = a.K / 16, nka = (KB + 3) / 4;
-  const int64_t tiles_x = nka, ntiles = tiles_x * ((a.R + 127) / 128);
+  const uint32_t kbl = t & 3, rl = t >> 2;
+  const uint32_t R = (uint32_t)a.R, KB = (uint32_t)(a.K / 16), nka = (KB + 3) / 4;
+  const uint32_t tiles_y = (R + 127) / 128;
+  const TileWalk walk(nka);
   uint32_t mask = 0;
   if constexpr (RHT) mask = rht_sign_mask(a.rht_seed);
   float g = 1.0f, amax = 0.0f;
@@ -146,33 +170,34 @@ __global__ void __launch_bounds__(256) k_quant_rows(QuantArgs a) {
   }
   const float g6 = __fmul_rn(6.0f, g), g4 = __fmul_rn(4.0f, g);
   float run_max = 0.0f;
+  const T* __restrict__ xp = reinterpret_cast<const T*>(a.x);
 
-  auto block_of = [&](int64_t tile, int h, int64_t& r, int64_t& kb) {
-    r = (tile / tiles_x) * 128 + rl + 64 * h;
-    kb = (tile % tiles_x) * 4 + kbl;
-  };
-  auto load = [&](int64_t tile, RawBlock<T> (&raw)[2]) {
+  auto load = [&](uint32_t ty, uint32_t tx, RawBlock<T> (&raw)[2]) {
+    const uint32_t kb = tx * 4 + kbl;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      int64_t r, kb;
-      block_of(tile, h, r, kb);
-      if (r < a.R && kb < KB) raw[h].load(reinterpret_cast<const T*>(a.x) + r * a.ld + kb * 16);
+      const uint32_t r = ty * 128 + rl + 64 * h;
+      if (r < R && kb < KB) raw[h].load(xp + (int64_t)r * a.ld + kb * 16);
       else raw[h].zero();
     }
   };
 
   RawBlock<T> cur[2], nxt[2];
-  int64_t tile = blockIdx.x;
-  if (tile < ntiles) load(tile, cur);
-  for (; tile < ntiles; tile += gridDim.x) {
-    if (tile + gridDim.x < ntiles) load(tile + gridDim.x, nxt);
+  uint32_t ty, tx;
+  walk.start(ty, tx);
+  if (ty < tiles_y) load(ty, tx, cur);
+  while (ty < tiles_y) {
+    uint32_t ny, nx;
+    walk.next(ty, tx, ny, nx);
+    if (ny < tiles_y) load(ny, nx, nxt);
     float v[2][16];
     bool valid[2];
-    int64_t r[2], kb[2];
+    uint32_t r[2];
+    const uint32_t kb = tx * 4 + kbl;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      block_of(tile, h, r[h], kb[h]);
-      valid[h] = r[h] < a.R && kb[h] < KB;
+      r[h] = ty * 128 + rl + 64 * h;
+      valid[h] = r[h] < R && kb < KB;
       cur[h].unpack(v[h]);
       if constexpr (RHT) rht16(v[h], mask);
     }
@@ -199,7 +224,7 @@ __global__ void __launch_bounds__(256) k_quant_rows(QuantArgs a) {
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         uint32_t u[16];
-        if constexpr (SR) sr_draws16(a.seed, a.offset, (uint64_t)(r[h] * a.K + kb[h] * 16), u);
+        if constexpr (SR) sr_draws16(a.seed, a.offset, (uint64_t)r[h] * (uint64_t)a.K + kb * 16, u);
         float s6, r6;
         sbyte[h] = block_scale(ab[h], g6, g, s6, r6);
         codes[h] = encode16<SR>(v[h], r6, u);
@@ -234,20 +259,22 @@ __global__ void __launch_bounds__(256) k_quant_rows(QuantArgs a) {
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         if (valid[h]) {
-          *reinterpret_cast<uint2*>(a.codes + r[h] * (a.K / 2) + kb[h] * 8) = codes[h];
+          *reinterpret_cast<uint2*>(a.codes + (int64_t)r[h] * (a.K / 2) + kb * 8) = codes[h];
           if (a.tdebug) {
-            float4* d = reinterpret_cast<float4*>(a.tdebug + r[h] * a.K + kb[h] * 16);
+            float4* d = reinterpret_cast<float4*>(a.tdebug + (int64_t)r[h] * a.K + kb * 16);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
               d[i] = make_float4(v[h][4 * i], v[h][4 * i + 1], v[h][4 * i + 2], v[h][4 * i + 3]);
           }
         }
-        a.scales[sf_offset(r[h], kb[h], nka)] = valid[h] ? (uint8_t)sbyte[h] : (uint8_t)0;
+        a.scales[sf_offset(r[h], kb, nka)] = valid[h] ? (uint8_t)sbyte[h] : (uint8_t)0;
       }
       if constexpr (B2D) __syncthreads();  // the exchange buffers are reused by the next tile
     }
 #pragma unroll
     for (int h = 0; h < 2; ++h) cur[h] = nxt[h];
+    ty = ny;
+    tx = nx;
   }
   if constexpr (AMAX_ONLY) cta_max_to_global(__float_as_uint(run_max), reinterpret_cast<unsigned int*>(a.amax_accum));
 }
@@ -289,9 +316,11 @@ __global__ void __launch_bounds__(256) k_quant_cols(QuantArgs a) {
   constexpr int NV = (64 * VPR) / 256;          // vectors per thread
   __shared__ __align__(16) uint8_t tile_s[64 * RB];
   const int t = threadIdx.x;
-  const int64_t Tt = a.R_in, N = a.C_in;  // input rows / cols
-  const int64_t K = Tt, KB = K / 16, nka = (KB + 3) / 4;
-  const int64_t tiles_x = (N + 127) / 128, ntiles = tiles_x * ((Tt + 63) / 64);
+  const uint32_t Tt = (uint32_t)a.R_in, N = (uint32_t)a.C_in;  // input rows / cols
+  const int64_t K = Tt;
+  const uint32_t KB = Tt / 16, nka = (KB + 3) / 4;
+  const uint32_t tiles_y = (Tt + 63) / 64;
+  const TileWalk walk((N + 127) / 128);
   const int np = t & 63, kbl = t >> 6;
   uint32_t mask = 0;
   if constexpr (RHT) mask = rht_sign_mask(a.rht_seed);
@@ -306,23 +335,25 @@ __global__ void __launch_bounds__(256) k_quant_cols(QuantArgs a) {
   }
   const float g6 = __fmul_rn(6.0f, g), g4 = __fmul_rn(4.0f, g);
   float run_max = 0.0f;
+  const T* __restrict__ xp = reinterpret_cast<const T*>(a.x);
 
-  auto load = [&](int64_t tile, uint4 (&raw)[NV]) {
-    const int64_t tok0 = (tile / tiles_x) * 64, n0 = (tile % tiles_x) * 128;
+  auto load = [&](uint32_t ty, uint32_t tx, uint4 (&raw)[NV]) {
+    const uint32_t tok0 = ty * 64, n0 = tx * 128;
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
-      int idx = t + 256 * i, row = idx / VPR, cv = idx % VPR;
-      int64_t col = n0 + (int64_t)cv * (16 / sizeof(T));
+      const int idx = t + 256 * i, row = idx / VPR, cv = idx % VPR;
+      const uint32_t col = n0 + (uint32_t)cv * (16 / sizeof(T));
       raw[i] = make_uint4(0, 0, 0, 0);
       if (tok0 + row < Tt && col < N)
-        raw[i] = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(a.x) + (tok0 + row) * a.ld + col));
+        raw[i] = __ldg(reinterpret_cast<const uint4*>(xp + (int64_t)(tok0 + row) * a.ld + col));
     }
   };
 
   uint4 raw[NV];
-  int64_t tile = blockIdx.x;
-  if (tile < ntiles) load(tile, raw);
-  for (; tile < ntiles; tile += gridDim.x) {
+  uint32_t ty, tx;
+  walk.start(ty, tx);
+  if (ty < tiles_y) load(ty, tx, raw);
+  while (ty < tiles_y) {
     __syncthreads();  // the previous tile's readers are done with tile_s
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
@@ -330,10 +361,12 @@ __global__ void __launch_bounds__(256) k_quant_cols(QuantArgs a) {
       *reinterpret_cast<uint4*>(tile_s + row * RB + cv * 16) = raw[i];
     }
     __syncthreads();
-    if (tile + gridDim.x < ntiles) load(tile + gridDim.x, raw);  // in flight during the encode
+    uint32_t ny, nx;
+    walk.next(ty, tx, ny, nx);
+    if (ny < tiles_y) load(ny, nx, raw);  // in flight during the encode
 
-    const int64_t n0 = (tile % tiles_x) * 128;
-    const int64_t kb = (tile / tiles_x) * 4 + kbl;
+    const uint32_t n0 = tx * 128;
+    const uint32_t kb = ty * 4 + kbl;
     float v[2][16];
 #pragma unroll
     for (int e = 0; e < 16; ++e) ColTile<T>::pair(tile_s, 16 * kbl + e, np, v[0][e], v[1][e]);
@@ -361,9 +394,9 @@ __global__ void __launch_bounds__(256) k_quant_cols(QuantArgs a) {
       float e6[2], e4[2];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const int64_t n = n0 + 2 * np + h;
+        const uint32_t n = n0 + 2 * np + h;
         uint32_t u[16];
-        if constexpr (SR) sr_draws16(a.seed, a.offset, (uint64_t)(n * K + kb * 16), u);
+        if constexpr (SR) sr_draws16(a.seed, a.offset, (uint64_t)n * (uint64_t)K + kb * 16, u);
         float s6, r6;
         sbyte[h] = block_scale(ab[h], g6, g, s6, r6);
         codes[h] = encode16<SR>(v[h], r6, u);
@@ -396,11 +429,11 @@ __global__ void __launch_bounds__(256) k_quant_cols(QuantArgs a) {
       }
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const int64_t n = n0 + 2 * np + h;
+        const uint32_t n = n0 + 2 * np + h;
         if (valid[h]) {
-          *reinterpret_cast<uint2*>(a.codes + n * (K / 2) + kb * 8) = codes[h];
+          *reinterpret_cast<uint2*>(a.codes + (int64_t)n * (K / 2) + kb * 8) = codes[h];
           if (a.tdebug) {
-            float4* d = reinterpret_cast<float4*>(a.tdebug + n * K + kb * 16);
+            float4* d = reinterpret_cast<float4*>(a.tdebug + (int64_t)n * K + kb * 16);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
               d[i] = make_float4(v[h][4 * i], v[h][4 * i + 1], v[h][4 * i + 2], v[h][4 * i + 3]);
@@ -409,6 +442,8 @@ __global__ void __launch_bounds__(256) k_quant_cols(QuantArgs a) {
         a.scales[sf_offset(n, kb, nka)] = valid[h] ? (uint8_t)sbyte[h] : (uint8_t)0;
       }
     }
+    ty = ny;
+    tx = nx;
   }
   if constexpr (AMAX_ONLY) cta_max_to_global(__float_as_uint(run_max), reinterpret_cast<unsigned int*>(a.amax_accum));
 }
