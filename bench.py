@@ -74,19 +74,50 @@ def ncu_traffic(kernel: str, src_hash: str):
 
 
 class ClockSampler:
-    """nvidia-smi samples (100 ms) of the SM clock and throttle reasons."""
+    """SM clock and throttle reasons sampled while the timed region runs:
+    NVML polled every ~2 ms from a thread (read-only queries), else
+    nvidia-smi at 100 ms."""
 
+    NAMES = (("hw_slowdown", "nvmlClocksEventReasonHwSlowdown"),
+             ("hw_thermal_slowdown", "nvmlClocksEventReasonHwThermalSlowdown"),
+             ("sw_thermal_slowdown", "nvmlClocksEventReasonSwThermalSlowdown"),
+             ("sw_power_cap", "nvmlClocksEventReasonSwPowerCap"))
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index: int):
         self.index = index
-        self.rows = []
-        self.proc = None
+        self.samples = []   # (sm_mhz, reasons set)
+        self.max_mhz = None
+        self.stop_flag = threading.Event()
         self.thread = None
+        self.proc = None
+        self.source = None
 
     def start(self):
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            h = pynvml.nvmlDeviceGetHandleByIndex(self.index)
+            self.max_mhz = float(pynvml.nvmlDeviceGetMaxClockInfo(h, pynvml.NVML_CLOCK_SM))
+            masks = [(n, getattr(pynvml, a)) for n, a in self.NAMES]
+            getr = getattr(pynvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                pynvml.nvmlDeviceGetCurrentClocksThrottleReasons
+
+            def poll():
+                while not self.stop_flag.is_set():
+                    mhz = float(pynvml.nvmlDeviceGetClockInfo(h, pynvml.NVML_CLOCK_SM))
+                    r = getr(h)
+                    self.samples.append((mhz, {n for n, m in masks if r & m}))
+                    time.sleep(0.002)
+
+            self.source = "nvml"
+            self.thread = threading.Thread(target=poll, daemon=True)
+            self.thread.start()
+            return
+        except Exception:
+            pass
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
                                           "--format=csv,noheader,nounits", "-lms", "100"], stdout=subprocess.PIPE,
@@ -94,14 +125,20 @@ class ClockSampler:
         except OSError:
             self.proc = None
             return
-        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.source = "nvidia-smi"
+
+        def read():
+            for line in self.proc.stdout:
+                r = [c.strip() for c in line.split(",")]
+                if len(r) >= 8 and r[0].replace(".", "").isdigit():
+                    self.max_mhz = float(r[1]) if r[1].replace(".", "").isdigit() else self.max_mhz
+                    self.samples.append((float(r[0]), {n for i, (n, _) in enumerate(self.NAMES) if r[4 + i] == "Active"}))
+
+        self.thread = threading.Thread(target=read, daemon=True)
         self.thread.start()
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.rows.append([c.strip() for c in line.split(",")])
-
     def stop(self):
+        self.stop_flag.set()
         if self.proc:
             self.proc.terminate()
             try:
@@ -110,12 +147,10 @@ class ClockSampler:
                 self.proc.kill()
         if self.thread:
             self.thread.join(timeout=5)
-        sm = [float(r[0]) for r in self.rows if len(r) >= 8 and r[0].replace(".", "").isdigit()]
-        mx = [float(r[1]) for r in self.rows if len(r) >= 8 and r[1].replace(".", "").isdigit()]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in self.rows if len(r) >= 8 for i in range(4) if r[4 + i] == "Active"})
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(sm)}
+        sm = [m for m, _ in self.samples]
+        reasons = sorted(set().union(*[r for _, r in self.samples])) if self.samples else []
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(sm), "source": self.source}
 
 
 def encode_rates(nv, x, w, dev, reps=24):
@@ -209,19 +244,13 @@ def run_ours(args, rank, world, local_rank):
             g.replay()
     nv.sync_check(stream)
 
-    sampler = ClockSampler(local_rank) if rank == 0 else None
-    if sampler:
-        sampler.start()
-    # untimed soak (about half a second of steps) so the clock samples see the GPU under load
-    soak_end = time.perf_counter() + 0.6
-    while time.perf_counter() < soak_end:
-        for _ in range(20):
-            g_step.replay()
-        torch.cuda.synchronize(dev)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if sampler:
+        sampler.start()
     for i in range(args.steps):
         flush.zero_()          # L2 flush between steps (outside the timed events)
         ev[i][0].record(stream)
@@ -391,7 +420,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="llama8b", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])

@@ -146,6 +146,27 @@ nvfp4_status nvfp4_rht_quantize(const void* x, nvfp4_dtype xt, int64_t rows, int
 nvfp4_status nvfp4_dequantize(const nvfp4_tensor* q, void* y, nvfp4_dtype yt, void* stream);
 
 /*
+ * nvfp4_transpose_2d - the NVFP4 tensor of x^T from that of x, for a tensor
+ * quantized with 2D 16x16 blocks (the Dgrad operand W^T from the weight's
+ * forward quantization; "NVIDIA Introduces a 4-Bit Pretraining Methodology
+ * Using NVFP4", "Method": 16x16 weight blocks keep the forward and backward
+ * quantization of W consistent).  A 16x16 block has one scale and its
+ * elements keep their codes under transposition, so the result is a pure
+ * repack: codes nibble-transposed, block scales re-laid out (padding 0),
+ * global_scale and amax copied.  With RNE rounding it equals, bit for bit,
+ * nvfp4_quantize of x^T with 2D blocks and the same scaling and amax; with
+ * stochastic rounding it keeps the codes drawn for x (the draws depend on
+ * the output orientation, so quantizing x^T would draw others): the same
+ * quantized weight serves both passes.
+ *   q   host struct with device buffers: rows x cols, quantized with
+ *       NVFP4_BLOCK_2D (not checked: a 1D-block tensor gives the scales of
+ *       every 16th row).  rows % 16 == 0, cols % 16 == 0.
+ *   qt  host struct with device buffers sized for cols x rows; written.
+ *       Must not share codes or scales with q.
+ */
+nvfp4_status nvfp4_transpose_2d(const nvfp4_tensor* q, nvfp4_tensor* qt, void* stream);
+
+/*
  * nvfp4_gemm - D = g_A * g_B * sum_k (a_mk * s^A_{m,k/16}) * (b_nk * s^B_{n,k/16})
  * on the tensor cores (block-scaled FP4 x FP4, FP32 accumulation), W4A4 as the
  * Nemotron 3 Ultra story says Blackwell runs natively.

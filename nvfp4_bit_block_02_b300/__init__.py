@@ -68,12 +68,13 @@ def lib() -> ctypes.CDLL:
         L.nvfp4_rht_quantize.argtypes = [P, ctypes.c_int, I64, I64, I64, ctypes.POINTER(CQuantConfig), U64, P,
                                          ctypes.POINTER(CTensor), P, P]
         L.nvfp4_dequantize.argtypes = [ctypes.POINTER(CTensor), P, ctypes.c_int, P]
+        L.nvfp4_transpose_2d.argtypes = [ctypes.POINTER(CTensor), ctypes.POINTER(CTensor), P]
         L.nvfp4_gemm.argtypes = [ctypes.POINTER(CTensor), ctypes.POINTER(CTensor), P, ctypes.c_int, I64, P]
         L.nvfp4_gemm_grouped.argtypes = [ctypes.c_int, ctypes.POINTER(CTensor), ctypes.POINTER(CTensor),
                                          ctypes.POINTER(ctypes.c_void_p), ctypes.c_int, P]
         L.nvfp4_sync_check.argtypes = [P]
-        for fn in ("nvfp4_quantize", "nvfp4_rht_quantize", "nvfp4_dequantize", "nvfp4_gemm", "nvfp4_gemm_grouped",
-                   "nvfp4_sync_check"):
+        for fn in ("nvfp4_quantize", "nvfp4_rht_quantize", "nvfp4_dequantize", "nvfp4_transpose_2d", "nvfp4_gemm",
+                   "nvfp4_gemm_grouped", "nvfp4_sync_check"):
             getattr(L, fn).restype = ctypes.c_int
         L.nvfp4_status_string.argtypes = [ctypes.c_int]
         L.nvfp4_status_string.restype = ctypes.c_char_p
@@ -194,6 +195,16 @@ def dequantize(q: NVFP4Tensor, dtype=torch.float32, out: torch.Tensor | None = N
     ct = q.c()
     _check(lib().nvfp4_dequantize(ctypes.byref(ct), _ptr(out), _dtype_code(out.dtype), _stream(stream)),
            "nvfp4_dequantize")
+    return out
+
+
+def transpose_2d(q: NVFP4Tensor, out: NVFP4Tensor | None = None, stream=None) -> NVFP4Tensor:
+    """nvfp4_transpose_2d: the NVFP4 tensor of x^T (cols x rows) from that of
+    x quantized with 2D 16x16 blocks (the Dgrad operand W^T), by repacking."""
+    if out is None:
+        out = NVFP4Tensor.empty(q.cols, q.rows, device=q.codes.device)
+    cq, co = q.c(), out.c()
+    _check(lib().nvfp4_transpose_2d(ctypes.byref(cq), ctypes.byref(co), _stream(stream)), "nvfp4_transpose_2d")
     return out
 
 

@@ -168,6 +168,23 @@ nvfp4_status nvfp4_rht_quantize(const void* x, nvfp4_dtype xt, int64_t rows, int
   return run_quantize(x, xt, rows, cols, ld, cfg, true, rht_seed, amax_in, out, transformed_debug, stream);
 }
 
+nvfp4_status nvfp4_transpose_2d(const nvfp4_tensor* q, nvfp4_tensor* qt, void* stream) {
+  nvfp4_status st = check_tensor_buffers(q, "q");
+  if (st != NVFP4_OK) return st;
+  st = check_tensor_buffers(qt, "qt");
+  if (st != NVFP4_OK) return st;
+  if (q->rows % 16 || q->cols % 16)
+    return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "a 2D-block tensor has rows and cols that are multiples of 16");
+  if (qt->rows != q->cols || qt->cols != q->rows) return fail(NVFP4_ERR_INVALID_ARG, "qt must be cols x rows of q");
+  if (q->rows > 0 && q->cols > 0 && (q->codes == qt->codes || q->scales == qt->scales))
+    return fail(NVFP4_ERR_INVALID_ARG, "qt must not share codes or scales with q");
+  if (q->rows / 64 > 65535) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "rows too large for the launch grid");
+  cudaError_t e = nvfp4::launch_transpose_2d(q->codes, q->scales, q->global_scale, q->amax, q->rows, q->cols,
+                                             qt->codes, qt->scales, qt->global_scale, qt->amax,
+                                             reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? NVFP4_OK : cuda_fail(e, "transpose_2d launch");
+}
+
 nvfp4_status nvfp4_dequantize(const nvfp4_tensor* q, void* y, nvfp4_dtype yt, void* stream) {
   nvfp4_status st = check_tensor_buffers(q, "q");
   if (st != NVFP4_OK) return st;

@@ -262,6 +262,19 @@ __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.
       : "r"(taddr)                                                                                                   \
       : "memory")
 
+// The registers written by a tcgen05.ld are only valid after tcgen05.wait::ld;
+// this empty asm names them as read-write after the wait, so no use of them
+// can be scheduled before it.
+#define NVFP4_LD_FENCE(r)                                                                                            \
+  asm volatile(""                                                                                                    \
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),    \
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),           \
+                 "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),         \
+                 "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),         \
+                 "+r"(r[29]), "+r"(r[30]), "+r"(r[31])                                                              \
+               :                                                                                                     \
+               : "memory")
+
 // K-major operand tile, 128-byte rows, 128B swizzle: 8-row atoms of 1024 B.
 __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
   return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
@@ -548,6 +561,8 @@ __device__ __forceinline__ void gemm_pairs(const Sched& sched, bool out_bf16, un
             NVFP4_LD32(taddr0 + c * 32, r0);
             NVFP4_LD32(taddr0 + c * 32 + 32, r1);
             tmem_ld_wait();
+            NVFP4_LD_FENCE(r0);
+            NVFP4_LD_FENCE(r1);
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               pk[16 * c + i] = pack_bf16(__fmul_rn(alpha, __uint_as_float(r0[2 * i])),
@@ -584,6 +599,7 @@ __device__ __forceinline__ void gemm_pairs(const Sched& sched, bool out_bf16, un
           if (active) {
             NVFP4_LD32(taddr0 + c * 32, r);
             tmem_ld_wait();
+            NVFP4_LD_FENCE(r);
           }
           if (c == 3) {
             tc_fence_before();

@@ -28,7 +28,7 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for required in ["nvfp4_quantize", "nvfp4_rht_quantize", "nvfp4_dequantize", "nvfp4_gemm",
+    for required in ["nvfp4_quantize", "nvfp4_rht_quantize", "nvfp4_dequantize", "nvfp4_transpose_2d", "nvfp4_gemm",
                      "nvfp4_gemm_grouped", "nvfp4_codes_bytes", "nvfp4_scales_bytes", "nvfp4_sync_check",
                      "nvfp4_status_string", "nvfp4_last_error"]:
         assert required in names
@@ -102,6 +102,18 @@ def test_gemm_argument_errors(L):
     assert L.nvfp4_gemm(ctypes.byref(A), ctypes.byref(B), D, 9, 256, None) == 1
     assert L.nvfp4_gemm_grouped(nv.MAX_GROUPS + 1, None, None, None, nv.BF16, None) == 1
     assert L.nvfp4_gemm_grouped(0, None, None, None, nv.BF16, None) == 0
+
+
+def test_transpose_2d_argument_errors(L):
+    q = _fake_tensor(64, 128)
+    qt = _fake_tensor(128, 64, base=0x800000)
+    assert L.nvfp4_transpose_2d(None, ctypes.byref(qt), None) == 1
+    assert L.nvfp4_transpose_2d(ctypes.byref(q), ctypes.byref(_fake_tensor(64, 128, base=0x800000)), None) == 1
+    assert L.nvfp4_transpose_2d(ctypes.byref(_fake_tensor(40, 128)), ctypes.byref(_fake_tensor(128, 40, base=0x800000)),
+                                None) == 2                                                  # rows % 16
+    assert L.nvfp4_transpose_2d(ctypes.byref(q), ctypes.byref(_fake_tensor(128, 64)), None) == 1   # shares buffers
+    mis = nv.CTensor(0x800008, 0x900000, 0xA00000, 0xA00100, 128, 64)
+    assert L.nvfp4_transpose_2d(ctypes.byref(q), ctypes.byref(mis), None) == 3
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device error path")
