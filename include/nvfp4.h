@@ -98,6 +98,9 @@ typedef struct {
   uint64_t offset;
 } nvfp4_quant_config;
 
+/* Largest `count` of the grouped calls. */
+#define NVFP4_MAX_GROUPS 128
+
 /* Byte sizes of the buffers of a rows x cols (K = cols) quantized tensor. */
 size_t nvfp4_codes_bytes(int64_t rows, int64_t cols);
 size_t nvfp4_scales_bytes(int64_t rows, int64_t cols); /* ceil(rows/128)*128 * ceil(cols/64)*4 */
@@ -118,6 +121,24 @@ size_t nvfp4_scales_bytes(int64_t rows, int64_t cols); /* ceil(rows/128)*128 * c
 nvfp4_status nvfp4_quantize(const void* x, nvfp4_dtype xt, int64_t rows, int64_t cols, int64_t ld,
                             const nvfp4_quant_config* cfg, const float* amax_in, nvfp4_tensor* out,
                             void* stream);
+
+/*
+ * nvfp4_quantize_grouped - `count` tensors quantized with one configuration
+ * in one amax launch and one encode launch (per 64 tensors): the per-expert
+ * tensors of a Mixture-of-Experts layer, each its own tensor with its own
+ * amax and g (the MoE workload of the recipe; Four-over-Six on expert
+ * weights per the hyper.ai story on the Nemotron 3 Ultra NVFP4 checkpoint).
+ *   x, rows, cols, ld, out: host arrays of `count` entries with the meaning
+ *   they have in nvfp4_quantize; the tensor amax is always computed
+ *   (amax_in = NULL).  Group e draws its stochastic-rounding bits with
+ *   offset cfg->offset + e, so experts never share draws.  The result of
+ *   group e equals nvfp4_quantize(x[e], ..., cfg with offset + e, NULL,
+ *   &out[e]) bit for bit.  count <= NVFP4_MAX_GROUPS; every group follows
+ *   the nvfp4_quantize shape rules; no RHT (use nvfp4_rht_quantize).
+ */
+nvfp4_status nvfp4_quantize_grouped(int count, const void* const* x, nvfp4_dtype xt, const int64_t* rows,
+                                    const int64_t* cols, const int64_t* ld, const nvfp4_quant_config* cfg,
+                                    nvfp4_tensor* out, void* stream);
 
 /*
  * nvfp4_rht_quantize - the Wgrad operand path: 16x16 Random Hadamard Transform
@@ -185,7 +206,6 @@ nvfp4_status nvfp4_gemm(const nvfp4_tensor* A, const nvfp4_tensor* B, void* D, n
  * array of `count` device pointers, each row-major [M_e][N_e] (ldd = N_e).
  * Every group follows the nvfp4_gemm shape rules; count <= NVFP4_MAX_GROUPS.
  */
-#define NVFP4_MAX_GROUPS 128
 nvfp4_status nvfp4_gemm_grouped(int count, const nvfp4_tensor* A, const nvfp4_tensor* B, void* const* D,
                                 nvfp4_dtype dt, void* stream);
 

@@ -69,12 +69,15 @@ def lib() -> ctypes.CDLL:
                                          ctypes.POINTER(CTensor), P, P]
         L.nvfp4_dequantize.argtypes = [ctypes.POINTER(CTensor), P, ctypes.c_int, P]
         L.nvfp4_transpose_2d.argtypes = [ctypes.POINTER(CTensor), ctypes.POINTER(CTensor), P]
+        L.nvfp4_quantize_grouped.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_void_p), ctypes.c_int,
+                                             ctypes.POINTER(I64), ctypes.POINTER(I64), ctypes.POINTER(I64),
+                                             ctypes.POINTER(CQuantConfig), ctypes.POINTER(CTensor), P]
         L.nvfp4_gemm.argtypes = [ctypes.POINTER(CTensor), ctypes.POINTER(CTensor), P, ctypes.c_int, I64, P]
         L.nvfp4_gemm_grouped.argtypes = [ctypes.c_int, ctypes.POINTER(CTensor), ctypes.POINTER(CTensor),
                                          ctypes.POINTER(ctypes.c_void_p), ctypes.c_int, P]
         L.nvfp4_sync_check.argtypes = [P]
-        for fn in ("nvfp4_quantize", "nvfp4_rht_quantize", "nvfp4_dequantize", "nvfp4_transpose_2d", "nvfp4_gemm",
-                   "nvfp4_gemm_grouped", "nvfp4_sync_check"):
+        for fn in ("nvfp4_quantize", "nvfp4_quantize_grouped", "nvfp4_rht_quantize", "nvfp4_dequantize",
+                   "nvfp4_transpose_2d", "nvfp4_gemm", "nvfp4_gemm_grouped", "nvfp4_sync_check"):
             getattr(L, fn).restype = ctypes.c_int
         L.nvfp4_status_string.argtypes = [ctypes.c_int]
         L.nvfp4_status_string.restype = ctypes.c_char_p
@@ -168,6 +171,29 @@ def quantize(x: torch.Tensor, *, block="1d", rounding="rne", scaling="max6", tra
     ct = out.c()
     _check(lib().nvfp4_quantize(_ptr(x), _dtype_code(x.dtype), rows, cols, ld, ctypes.byref(cfg), _ptr(amax),
                                 ctypes.byref(ct), _stream(stream)), "nvfp4_quantize")
+    return out
+
+
+def quantize_grouped(xs: list, *, block="1d", rounding="rne", scaling="max6", transpose=False, seed=0, offset=0,
+                     out: list | None = None, stream=None) -> list:
+    """nvfp4_quantize_grouped: every tensor of ``xs`` (same dtype) quantized
+    with its own amax, one amax and one encode launch per 64 tensors; group
+    e draws SR bits at offset + e."""
+    n = len(xs)
+    if n == 0:
+        return []
+    dims = [_prep_input(x) for x in xs]
+    if out is None:
+        out = [NVFP4Tensor.empty(c if transpose else r, r if transpose else c, device=xs[0].device)
+               for (r, c, _) in dims]
+    cfg = _config(block, rounding, scaling, transpose, seed, offset)
+    X = (ctypes.c_void_p * n)(*[x.data_ptr() for x in xs])
+    R = (ctypes.c_int64 * n)(*[d[0] for d in dims])
+    C = (ctypes.c_int64 * n)(*[d[1] for d in dims])
+    L = (ctypes.c_int64 * n)(*[d[2] for d in dims])
+    O = (CTensor * n)(*[o.c() for o in out])
+    _check(lib().nvfp4_quantize_grouped(n, X, _dtype_code(xs[0].dtype), R, C, L, ctypes.byref(cfg), O,
+                                        _stream(stream)), "nvfp4_quantize_grouped")
     return out
 
 

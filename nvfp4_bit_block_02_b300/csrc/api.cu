@@ -168,6 +168,60 @@ nvfp4_status nvfp4_rht_quantize(const void* x, nvfp4_dtype xt, int64_t rows, int
   return run_quantize(x, xt, rows, cols, ld, cfg, true, rht_seed, amax_in, out, transformed_debug, stream);
 }
 
+nvfp4_status nvfp4_quantize_grouped(int count, const void* const* x, nvfp4_dtype xt, const int64_t* rows,
+                                    const int64_t* cols, const int64_t* ld, const nvfp4_quant_config* cfg,
+                                    nvfp4_tensor* out, void* stream) {
+  if (count < 0 || count > NVFP4_MAX_GROUPS)
+    return fail(NVFP4_ERR_INVALID_ARG, "count must be in [0, " + std::to_string(NVFP4_MAX_GROUPS) + "]");
+  if (count == 0) return NVFP4_OK;
+  if (!x || !rows || !cols || !ld || !out) return fail(NVFP4_ERR_INVALID_ARG, "a host array is NULL");
+  for (int e = 0; e < count; ++e) {
+    nvfp4_status st = check_quantize(x[e], xt, rows[e], cols[e], ld[e], cfg, &out[e], false);
+    if (st != NVFP4_OK) return fail(st, "group " + std::to_string(e) + ": " + g_last_error);
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const bool bf16 = xt == NVFP4_BF16, tr = cfg->transpose != 0, b2d = cfg->block == NVFP4_BLOCK_2D,
+             sr = cfg->round == NVFP4_ROUND_STOCHASTIC, f46 = cfg->scaling == NVFP4_SCALE_FOUR_OVER_SIX;
+  nvfp4::GroupQuant gq{};  // kernel parameters of one launch (~9 KB, copied at launch)
+  nvfp4::GroupQuant* gp = &gq;
+  int n = 0;
+  auto flush = [&]() -> nvfp4_status {
+    if (n == 0) return NVFP4_OK;
+    gp->count = n;
+    cudaError_t e = nvfp4::launch_quantize_grouped(*gp, bf16, tr, b2d, sr, f46, true, s);
+    n = 0;
+    return e == cudaSuccess ? NVFP4_OK : cuda_fail(e, "grouped quantize launch");
+  };
+  nvfp4_status st = NVFP4_OK;
+  for (int e = 0; e < count && st == NVFP4_OK; ++e) {
+    nvfp4_tensor* o = &out[e];
+    if (o->rows == 0 || o->cols == 0) {
+      cudaError_t ce = nvfp4::launch_empty_scalars(o->amax, o->global_scale, s);
+      if (ce != cudaSuccess) st = cuda_fail(ce, "empty-tensor scalars");
+      continue;
+    }
+    nvfp4::QuantArgs& a = gp->a[n++];
+    a = nvfp4::QuantArgs{};
+    a.x = x[e];
+    a.R_in = rows[e];
+    a.C_in = cols[e];
+    a.ld = ld[e];
+    a.R = o->rows;
+    a.K = o->cols;
+    a.amax_in = o->amax;
+    a.amax_out = o->amax;
+    a.amax_accum = o->amax;
+    a.g_out = o->global_scale;
+    a.codes = o->codes;
+    a.scales = o->scales;
+    a.seed = cfg->seed;
+    a.offset = cfg->offset + (uint64_t)e;
+    if (n == nvfp4::kQuantGroups) st = flush();
+  }
+  if (st == NVFP4_OK) st = flush();
+  return st;
+}
+
 nvfp4_status nvfp4_transpose_2d(const nvfp4_tensor* q, nvfp4_tensor* qt, void* stream) {
   nvfp4_status st = check_tensor_buffers(q, "q");
   if (st != NVFP4_OK) return st;

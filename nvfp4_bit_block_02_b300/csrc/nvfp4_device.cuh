@@ -1,9 +1,10 @@
 // Device helpers of the NVFP4 kernels (sm_103a).  Every fp32 operation that
 // decides a code or a scale is an explicit IEEE intrinsic (__fmul_rn,
-// __fmul2_rn, __fdiv_rn, __frcp_rn, __fadd_rn, __fsub_rn, and one __fmaf_ru
-// whose exact result is rounded upward on purpose) so that the compiler
-// cannot contract or reorder it; the encoder's results are therefore fixed
-// bit for bit by the sequence written in nvfp4.h.
+// __fdiv_rn, __frcp_rn, __fadd_rn, __fsub_rn, and one __fmaf_ru whose exact
+// result is rounded upward on purpose) or a packed PTX multiply with an
+// explicit rounding mode (mul.rn.f32x2) whose result feeds only a conversion,
+// so that the compiler cannot contract or reorder it; the encoder's results
+// are therefore fixed bit for bit by the sequence written in nvfp4.h.
 #pragma once
 #include <cstdint>
 #include <cuda_bf16.h>
@@ -166,6 +167,19 @@ __device__ __forceinline__ uint32_t block_scale(float amax_b, float mg, float g,
   return b;
 }
 
+// Packed fp32x2 multiply, each lane an IEEE round-to-nearest-even product
+// with subnormals kept (PTX with an explicit rounding mode).  Used only where
+// the product feeds a conversion, never an addition, so no fused
+// multiply-add can form from it.
+__device__ __forceinline__ float2 mul2_rn(float2 a, float2 b) {
+  float2 r;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
 // Encode 16 values with block reciprocal rcp into two 32-bit words of codes.
 // The products are paired into packed fp32x2 multiplies (each lane an IEEE
 // round-to-nearest product, the same value as a scalar multiply).
@@ -175,7 +189,7 @@ __device__ __forceinline__ uint2 encode16(const float v[16], float rcp, const ui
   const float2 rr = make_float2(rcp, rcp);
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const float2 p = __fmul2_rn(make_float2(v[2 * i], v[2 * i + 1]), rr);
+    const float2 p = mul2_rn(make_float2(v[2 * i], v[2 * i + 1]), rr);
     q[2 * i] = p.x;
     q[2 * i + 1] = p.y;
   }

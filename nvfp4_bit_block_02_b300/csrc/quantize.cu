@@ -64,6 +64,46 @@ __global__ void __launch_bounds__(256) k_amax(const T* __restrict__ x, int64_t r
   cta_max_to_global(m, out);
 }
 
+// Loop-safe CTA max + one atomicMax (callable repeatedly in a CTA-uniform loop).
+__device__ __forceinline__ void cta_max_atomic(uint32_t m, unsigned int* out) {
+  __shared__ uint32_t red[8];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  m = __reduce_max_sync(0xFFFFFFFFu, m);
+  __syncthreads();  // the previous call's reads of red[] are done
+  if (lane == 0) red[warp] = m;
+  __syncthreads();
+  if (warp == 0) {
+    m = lane < (int)(blockDim.x >> 5) ? red[lane] : 0u;
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    if (lane == 0 && m) atomicMax(out, m);
+  }
+}
+
+// Grouped tensor amax: tiles of amax_rows[e] input rows of group e; a CTA
+// reduces a tile and folds it into the group's accumulator.
+template <typename T>
+__global__ void __launch_bounds__(256) k_amax_grouped(const __grid_constant__ GroupQuant g) {
+  constexpr int VEC = 16 / sizeof(T);
+  const uint32_t total = g.amax_start[g.count];
+  for (uint32_t t = blockIdx.x; t < total; t += gridDim.x) {
+    uint32_t e = 0;
+    while (t >= g.amax_start[e + 1]) ++e;
+    const QuantArgs& a = g.a[e];
+    const int64_t nvec = a.C_in / VEC, ldv = a.ld / VEC;
+    const int64_t r0 = (int64_t)(t - g.amax_start[e]) * g.amax_rows[e];
+    const int64_t r1 = min(r0 + (int64_t)g.amax_rows[e], a.R_in);
+    const uint4* base = reinterpret_cast<const uint4*>(a.x);
+    uint32_t m = 0;
+    for (int64_t r = r0; r < r1; ++r)
+      for (int64_t v = threadIdx.x; v < nvec; v += blockDim.x) m = max(m, absmax_bits(__ldg(base + r * ldv + v), T()));
+    cta_max_atomic(m, reinterpret_cast<unsigned int*>(a.amax_accum));
+  }
+}
+
+__global__ void k_zero_group_amax(const __grid_constant__ GroupQuant g) {
+  if ((int)threadIdx.x < g.count) *g.a[threadIdx.x].amax_accum = 0.0f;
+}
+
 // ---------------------------------------------------------------------------
 // Raw 16-element block loads (kept packed until used, so a thread can hold
 // the next tile's blocks in flight while it encodes the current one).
@@ -140,6 +180,54 @@ struct TileWalk {
   }
 };
 
+// Tile sources of the persistent encoders.  OneTensor walks one tensor's
+// tile grid with TileWalk; Groups walks the concatenated tile lists of up to
+// kQuantGroups tensors (tile_start[] prefix sums), each with its own args.
+struct OneTensor {
+  static constexpr bool kGrouped = false;
+  struct Ref {
+    uint32_t ty, tx;
+  };
+  const QuantArgs& a;
+  uint32_t tiles_y;
+  TileWalk walk;
+  __device__ OneTensor(const QuantArgs& args, uint32_t tiles_x, uint32_t ty) : a(args), tiles_y(ty), walk(tiles_x) {}
+  __device__ const QuantArgs& args(const Ref&) const { return a; }
+  __device__ bool first(Ref& r) const {
+    walk.start(r.ty, r.tx);
+    return r.ty < tiles_y;
+  }
+  __device__ bool next(const Ref& c, Ref& n) const {
+    walk.next(c.ty, c.tx, n.ty, n.tx);
+    return n.ty < tiles_y;
+  }
+};
+
+struct Groups {
+  static constexpr bool kGrouped = true;
+  struct Ref {
+    uint32_t t, e, ty, tx;
+  };
+  const GroupQuant& g;
+  __device__ explicit Groups(const GroupQuant& gq) : g(gq) {}
+  __device__ const QuantArgs& args(const Ref& r) const { return g.a[r.e]; }
+  __device__ bool locate(uint32_t t, Ref& r) const {
+    if (t >= g.tile_start[g.count]) return false;
+    uint32_t e = 0;
+    while (t >= g.tile_start[e + 1]) ++e;
+    const uint32_t local = t - g.tile_start[e];
+    r.t = t;
+    r.e = e;
+    r.ty = local / g.tiles_x[e];
+    r.tx = local % g.tiles_x[e];
+    return true;
+  }
+  __device__ bool first(Ref& r) const { return locate(blockIdx.x, r); }
+  __device__ bool next(const Ref& c, Ref& n) const { return locate(c.t + gridDim.x, n); }
+  // the first tile of a group publishes its g and amax
+  __device__ bool owns_scalars(const Ref& r) const { return r.t == g.tile_start[r.e]; }
+};
+
 // ---------------------------------------------------------------------------
 // Row-wise encoder: K = cols.  Persistent: CTA b handles tiles b, b + G, ...
 // of 128 rows x 4 blocks; thread t owns blocks (row t/4 + 64h, block t%4) of
@@ -148,55 +236,60 @@ struct TileWalk {
 // 2i+1 (lane bits 2..4 = row bits 0..2).  Index arithmetic is 32-bit (rows
 // and 16-element blocks each fit in 31 bits); byte offsets are 64-bit.
 // ---------------------------------------------------------------------------
-template <typename T, bool B2D, bool SR, bool F46, bool RHT, bool AMAX_ONLY>
-__global__ void __launch_bounds__(256) k_quant_rows(QuantArgs a) {
+template <typename T, bool B2D, bool SR, bool F46, bool RHT, bool AMAX_ONLY, class Src>
+__device__ __forceinline__ void quant_rows_body(const Src& src, const QuantArgs& a0) {
   __shared__ float xw[8][2][4];    // cross-warp exchange for 2D tiles
   __shared__ float xw4[8][2][4];
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const uint32_t kbl = t & 3, rl = t >> 2;
-  const uint32_t R = (uint32_t)a.R, KB = (uint32_t)(a.K / 16), nka = (KB + 3) / 4;
-  const uint32_t tiles_y = (R + 127) / 128;
-  const TileWalk walk(nka);
   uint32_t mask = 0;
-  if constexpr (RHT) mask = rht_sign_mask(a.rht_seed);
-  float g = 1.0f, amax = 0.0f;
-  if constexpr (!AMAX_ONLY) {
-    amax = *a.amax_in;
+  if constexpr (RHT) mask = rht_sign_mask(a0.rht_seed);
+  // per-tensor scale: once for one tensor, per tile (its group's) for groups
+  float g = 1.0f, g6 = 6.0f, g4 = 4.0f;
+  auto set_scale = [&](const QuantArgs& a, bool publish) {
+    const float amax = *a.amax_in;
     g = global_scale(amax);
-    if (blockIdx.x == 0 && t == 0) {
+    g6 = __fmul_rn(6.0f, g);
+    g4 = __fmul_rn(4.0f, g);
+    if (publish && t == 0) {
       *a.g_out = g;
       if (a.amax_out != a.amax_in) *a.amax_out = amax;
     }
-  }
-  const float g6 = __fmul_rn(6.0f, g), g4 = __fmul_rn(4.0f, g);
+  };
+  if constexpr (!AMAX_ONLY && !Src::kGrouped) set_scale(a0, blockIdx.x == 0);
   float run_max = 0.0f;
-  const T* __restrict__ xp = reinterpret_cast<const T*>(a.x);
 
-  auto load = [&](uint32_t ty, uint32_t tx, RawBlock<T> (&raw)[2]) {
-    const uint32_t kb = tx * 4 + kbl;
+  auto load = [&](const typename Src::Ref& ref, RawBlock<T> (&raw)[2]) {
+    const QuantArgs& a = src.args(ref);
+    const uint32_t R = (uint32_t)a.R, KB = (uint32_t)(a.K / 16);
+    const uint32_t kb = ref.tx * 4 + kbl;
+    const T* __restrict__ xp = reinterpret_cast<const T*>(a.x);
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const uint32_t r = ty * 128 + rl + 64 * h;
+      const uint32_t r = ref.ty * 128 + rl + 64 * h;
       if (r < R && kb < KB) raw[h].load(xp + (int64_t)r * a.ld + kb * 16);
       else raw[h].zero();
     }
   };
 
   RawBlock<T> cur[2], nxt[2];
-  uint32_t ty, tx;
-  walk.start(ty, tx);
-  if (ty < tiles_y) load(ty, tx, cur);
-  while (ty < tiles_y) {
-    uint32_t ny, nx;
-    walk.next(ty, tx, ny, nx);
-    if (ny < tiles_y) load(ny, nx, nxt);
+  typename Src::Ref ref;
+  bool have = src.first(ref);
+  if (have) load(ref, cur);
+  while (have) {
+    typename Src::Ref nref;
+    const bool have_next = src.next(ref, nref);
+    if (have_next) load(nref, nxt);
+    const QuantArgs& a = src.args(ref);
+    const uint32_t R = (uint32_t)a.R, KB = (uint32_t)(a.K / 16), nka = (KB + 3) / 4;
+    if constexpr (!AMAX_ONLY && Src::kGrouped) set_scale(a, src.owns_scalars(ref));
     float v[2][16];
     bool valid[2];
     uint32_t r[2];
-    const uint32_t kb = tx * 4 + kbl;
+    const uint32_t kb = ref.tx * 4 + kbl;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      r[h] = ty * 128 + rl + 64 * h;
+      r[h] = ref.ty * 128 + rl + 64 * h;
       valid[h] = r[h] < R && kb < KB;
       cur[h].unpack(v[h]);
       if constexpr (RHT) rht16(v[h], mask);
@@ -219,21 +312,27 @@ __global__ void __launch_bounds__(256) k_quant_rows(QuantArgs a) {
 #pragma unroll
         for (int h = 0; h < 2; ++h) ab[h] = fmaxf(ab[h], xw[warp ^ 1][h][kbl]);
       }
-      uint2 codes[2];
-      uint32_t sbyte[2];
+      uint2 codes[2], c4[2];
+      uint32_t sbyte[2], b4[2];
+      float s6[2], s4[2];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         uint32_t u[16];
         if constexpr (SR) sr_draws16(a.seed, a.offset, (uint64_t)r[h] * (uint64_t)a.K + kb * 16, u);
-        float s6, r6;
-        sbyte[h] = block_scale(ab[h], g6, g, s6, r6);
+        float r6;
+        sbyte[h] = block_scale(ab[h], g6, g, s6[h], r6);
         codes[h] = encode16<SR>(v[h], r6, u);
         if constexpr (F46) {
-          float s4, r4;
-          uint32_t b4 = block_scale(ab[h], g4, g, s4, r4);
-          uint2 c4 = encode16<SR>(v[h], r4, u);
-          float e6 = block_sq_err16(v[h], codes[h], s6, g);
-          float e4 = block_sq_err16(v[h], c4, s4, g);
+          float r4;
+          b4[h] = block_scale(ab[h], g4, g, s4[h], r4);
+          c4[h] = encode16<SR>(v[h], r4, u);
+        }
+      }
+      if constexpr (F46) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          float e6 = block_sq_err16(v[h], codes[h], s6[h], g);
+          float e4 = block_sq_err16(v[h], c4[h], s4[h], g);
           if constexpr (B2D) {
 #pragma unroll
             for (int o = 4; o <= 16; o <<= 1) {
@@ -251,8 +350,8 @@ __global__ void __launch_bounds__(256) k_quant_rows(QuantArgs a) {
             e4 = __fadd_rn(e4, xw4[warp ^ 1][h][kbl]);
           }
           if (e4 < e6) {
-            codes[h] = c4;
-            sbyte[h] = b4;
+            codes[h] = c4[h];
+            sbyte[h] = b4[h];
           }
         }
       }
@@ -273,10 +372,23 @@ __global__ void __launch_bounds__(256) k_quant_rows(QuantArgs a) {
     }
 #pragma unroll
     for (int h = 0; h < 2; ++h) cur[h] = nxt[h];
-    ty = ny;
-    tx = nx;
+    ref = nref;
+    have = have_next;
   }
-  if constexpr (AMAX_ONLY) cta_max_to_global(__float_as_uint(run_max), reinterpret_cast<unsigned int*>(a.amax_accum));
+  if constexpr (AMAX_ONLY) cta_max_to_global(__float_as_uint(run_max), reinterpret_cast<unsigned int*>(a0.amax_accum));
+}
+
+template <typename T, bool B2D, bool SR, bool F46, bool RHT, bool AMAX_ONLY>
+__global__ void __launch_bounds__(256) k_quant_rows(QuantArgs a) {
+  const uint32_t KB = (uint32_t)(a.K / 16);
+  const OneTensor src(a, (KB + 3) / 4, (uint32_t)((a.R + 127) / 128));
+  quant_rows_body<T, B2D, SR, F46, RHT, AMAX_ONLY>(src, a);
+}
+
+template <typename T, bool B2D, bool SR, bool F46>
+__global__ void __launch_bounds__(256) k_quant_rows_grouped(const __grid_constant__ GroupQuant g) {
+  const Groups src(g);
+  quant_rows_body<T, B2D, SR, F46, false, false>(src, g.a[0]);
 }
 
 // ---------------------------------------------------------------------------
@@ -309,36 +421,35 @@ struct ColTile<float> {
   }
 };
 
-template <typename T, bool B2D, bool SR, bool F46, bool RHT, bool AMAX_ONLY>
-__global__ void __launch_bounds__(256) k_quant_cols(QuantArgs a) {
+template <typename T, bool B2D, bool SR, bool F46, bool RHT, bool AMAX_ONLY, class Src>
+__device__ __forceinline__ void quant_cols_body(const Src& src, const QuantArgs& a0) {
   constexpr int RB = ColTile<T>::kRowBytes;
   constexpr int VPR = RB / 16;                  // 16-byte vectors per tile row
   constexpr int NV = (64 * VPR) / 256;          // vectors per thread
   __shared__ __align__(16) uint8_t tile_s[64 * RB];
   const int t = threadIdx.x;
-  const uint32_t Tt = (uint32_t)a.R_in, N = (uint32_t)a.C_in;  // input rows / cols
-  const int64_t K = Tt;
-  const uint32_t KB = Tt / 16, nka = (KB + 3) / 4;
-  const uint32_t tiles_y = (Tt + 63) / 64;
-  const TileWalk walk((N + 127) / 128);
   const int np = t & 63, kbl = t >> 6;
   uint32_t mask = 0;
-  if constexpr (RHT) mask = rht_sign_mask(a.rht_seed);
-  float g = 1.0f;
-  if constexpr (!AMAX_ONLY) {
+  if constexpr (RHT) mask = rht_sign_mask(a0.rht_seed);
+  float g = 1.0f, g6 = 6.0f, g4 = 4.0f;
+  auto set_scale = [&](const QuantArgs& a, bool publish) {
     const float amax = *a.amax_in;
     g = global_scale(amax);
-    if (blockIdx.x == 0 && t == 0) {
+    g6 = __fmul_rn(6.0f, g);
+    g4 = __fmul_rn(4.0f, g);
+    if (publish && t == 0) {
       *a.g_out = g;
       if (a.amax_out != a.amax_in) *a.amax_out = amax;
     }
-  }
-  const float g6 = __fmul_rn(6.0f, g), g4 = __fmul_rn(4.0f, g);
+  };
+  if constexpr (!AMAX_ONLY && !Src::kGrouped) set_scale(a0, blockIdx.x == 0);
   float run_max = 0.0f;
-  const T* __restrict__ xp = reinterpret_cast<const T*>(a.x);
 
-  auto load = [&](uint32_t ty, uint32_t tx, uint4 (&raw)[NV]) {
-    const uint32_t tok0 = ty * 64, n0 = tx * 128;
+  auto load = [&](const typename Src::Ref& ref, uint4 (&raw)[NV]) {
+    const QuantArgs& a = src.args(ref);
+    const uint32_t Tt = (uint32_t)a.R_in, N = (uint32_t)a.C_in;
+    const T* __restrict__ xp = reinterpret_cast<const T*>(a.x);
+    const uint32_t tok0 = ref.ty * 64, n0 = ref.tx * 128;
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
       const int idx = t + 256 * i, row = idx / VPR, cv = idx % VPR;
@@ -350,10 +461,10 @@ __global__ void __launch_bounds__(256) k_quant_cols(QuantArgs a) {
   };
 
   uint4 raw[NV];
-  uint32_t ty, tx;
-  walk.start(ty, tx);
-  if (ty < tiles_y) load(ty, tx, raw);
-  while (ty < tiles_y) {
+  typename Src::Ref ref;
+  bool have = src.first(ref);
+  if (have) load(ref, raw);
+  while (have) {
     __syncthreads();  // the previous tile's readers are done with tile_s
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
@@ -361,12 +472,17 @@ __global__ void __launch_bounds__(256) k_quant_cols(QuantArgs a) {
       *reinterpret_cast<uint4*>(tile_s + row * RB + cv * 16) = raw[i];
     }
     __syncthreads();
-    uint32_t ny, nx;
-    walk.next(ty, tx, ny, nx);
-    if (ny < tiles_y) load(ny, nx, raw);  // in flight during the encode
+    typename Src::Ref nref;
+    const bool have_next = src.next(ref, nref);
+    if (have_next) load(nref, raw);  // in flight during the encode
 
-    const uint32_t n0 = tx * 128;
-    const uint32_t kb = ty * 4 + kbl;
+    const QuantArgs& a = src.args(ref);
+    const uint32_t Tt = (uint32_t)a.R_in, N = (uint32_t)a.C_in;
+    const int64_t K = Tt;
+    const uint32_t KB = Tt / 16, nka = (KB + 3) / 4;
+    if constexpr (!AMAX_ONLY && Src::kGrouped) set_scale(a, src.owns_scalars(ref));
+    const uint32_t n0 = ref.tx * 128;
+    const uint32_t kb = ref.ty * 4 + kbl;
     float v[2][16];
 #pragma unroll
     for (int e = 0; e < 16; ++e) ColTile<T>::pair(tile_s, 16 * kbl + e, np, v[0][e], v[1][e]);
@@ -391,7 +507,7 @@ __global__ void __launch_bounds__(256) k_quant_cols(QuantArgs a) {
       }
       uint2 codes[2], c4[2];
       uint32_t sbyte[2], b4[2];
-      float e6[2], e4[2];
+      float e6[2], e4[2], s6v[2], s4v[2];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const uint32_t n = n0 + 2 * np + h;
@@ -401,14 +517,18 @@ __global__ void __launch_bounds__(256) k_quant_cols(QuantArgs a) {
         sbyte[h] = block_scale(ab[h], g6, g, s6, r6);
         codes[h] = encode16<SR>(v[h], r6, u);
         if constexpr (F46) {
-          float s4, r4;
-          b4[h] = block_scale(ab[h], g4, g, s4, r4);
+          float r4;
+          b4[h] = block_scale(ab[h], g4, g, s4v[h], r4);
           c4[h] = encode16<SR>(v[h], r4, u);
-          e6[h] = block_sq_err16(v[h], codes[h], s6, g);
-          e4[h] = block_sq_err16(v[h], c4[h], s4, g);
+          s6v[h] = s6;
         }
       }
       if constexpr (F46) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          e6[h] = block_sq_err16(v[h], codes[h], s6v[h], g);
+          e4[h] = block_sq_err16(v[h], c4[h], s4v[h], g);
+        }
         if constexpr (B2D) {
           // tile rows 2p, 2p+1 are this thread's pair; then pairs of pairs ...
           float s6 = __fadd_rn(e6[0], e6[1]), s4 = __fadd_rn(e4[0], e4[1]);
@@ -442,11 +562,24 @@ __global__ void __launch_bounds__(256) k_quant_cols(QuantArgs a) {
         a.scales[sf_offset(n, kb, nka)] = valid[h] ? (uint8_t)sbyte[h] : (uint8_t)0;
       }
     }
-    ty = ny;
-    tx = nx;
+    ref = nref;
+    have = have_next;
   }
-  if constexpr (AMAX_ONLY) cta_max_to_global(__float_as_uint(run_max), reinterpret_cast<unsigned int*>(a.amax_accum));
+  if constexpr (AMAX_ONLY) cta_max_to_global(__float_as_uint(run_max), reinterpret_cast<unsigned int*>(a0.amax_accum));
 }
+
+template <typename T, bool B2D, bool SR, bool F46, bool RHT, bool AMAX_ONLY>
+__global__ void __launch_bounds__(256) k_quant_cols(QuantArgs a) {
+  const OneTensor src(a, (uint32_t)((a.C_in + 127) / 128), (uint32_t)((a.R_in + 63) / 64));
+  quant_cols_body<T, B2D, SR, F46, RHT, AMAX_ONLY>(src, a);
+}
+
+template <typename T, bool B2D, bool SR, bool F46>
+__global__ void __launch_bounds__(256) k_quant_cols_grouped(const __grid_constant__ GroupQuant g) {
+  const Groups src(g);
+  quant_cols_body<T, B2D, SR, F46, false, false>(src, g.a[0]);
+}
+
 
 // ---------------------------------------------------------------------------
 // Decoder: one thread per block of 16 (grid-stride).
@@ -579,6 +712,73 @@ static void dispatch_opts(const QuantArgs& a, bool transpose, bool b2d, bool sr,
       else launch_q<T, false, false, false, RHT, AO>(a, transpose, s);
     }
   }
+}
+
+template <typename T, bool B2D, bool SR, bool F46>
+static void launch_qg(const GroupQuant& g, bool transpose, cudaStream_t s) {
+  const uint32_t tiles = g.tile_start[g.count];
+  if (!transpose) {
+    auto k = k_quant_rows_grouped<T, B2D, SR, F46>;
+    static unsigned cap = 0;
+    if (!cap) cap = persistent_grid(k, (int64_t)1 << 40);
+    k<<<tiles < cap ? tiles : cap, 256, 0, s>>>(g);
+  } else {
+    auto k = k_quant_cols_grouped<T, B2D, SR, F46>;
+    static unsigned cap = 0;
+    if (!cap) cap = persistent_grid(k, (int64_t)1 << 40);
+    k<<<tiles < cap ? tiles : cap, 256, 0, s>>>(g);
+  }
+}
+
+template <typename T>
+static void dispatch_grouped(const GroupQuant& g, bool transpose, bool b2d, bool sr, bool f46, cudaStream_t s) {
+  if (b2d) {
+    if (sr) {
+      if (f46) launch_qg<T, true, true, true>(g, transpose, s);
+      else launch_qg<T, true, true, false>(g, transpose, s);
+    } else {
+      if (f46) launch_qg<T, true, false, true>(g, transpose, s);
+      else launch_qg<T, true, false, false>(g, transpose, s);
+    }
+  } else {
+    if (sr) {
+      if (f46) launch_qg<T, false, true, true>(g, transpose, s);
+      else launch_qg<T, false, true, false>(g, transpose, s);
+    } else {
+      if (f46) launch_qg<T, false, false, true>(g, transpose, s);
+      else launch_qg<T, false, false, false>(g, transpose, s);
+    }
+  }
+}
+
+cudaError_t launch_quantize_grouped(GroupQuant& g, bool bf16, bool transpose, bool b2d, bool sr, bool f46,
+                                    bool compute_amax, cudaStream_t s) {
+  if (g.count <= 0) return cudaSuccess;
+  const int64_t es = bf16 ? 2 : 4;
+  uint32_t tiles = 0, atiles = 0;
+  for (int e = 0; e < g.count; ++e) {
+    const QuantArgs& a = g.a[e];
+    g.tiles_x[e] = transpose ? (uint32_t)((a.C_in + 127) / 128) : (uint32_t)((a.K / 16 + 3) / 4);
+    const uint32_t tiles_y = transpose ? (uint32_t)((a.R_in + 63) / 64) : (uint32_t)((a.R + 127) / 128);
+    g.tile_start[e] = tiles;
+    tiles += g.tiles_x[e] * tiles_y;
+    const int64_t row_bytes = a.C_in * es;
+    g.amax_rows[e] = (uint32_t)(row_bytes >= 65536 ? 1 : 65536 / row_bytes);
+    g.amax_start[e] = atiles;
+    atiles += (uint32_t)((a.R_in + g.amax_rows[e] - 1) / g.amax_rows[e]);
+  }
+  g.tile_start[g.count] = tiles;
+  g.amax_start[g.count] = atiles;
+  if (compute_amax) {
+    k_zero_group_amax<<<1, kQuantGroups, 0, s>>>(g);
+    const unsigned cap = (unsigned)num_sms() * 8;
+    const unsigned grid = atiles < cap ? atiles : cap;
+    if (bf16) k_amax_grouped<__nv_bfloat16><<<grid, 256, 0, s>>>(g);
+    else k_amax_grouped<float><<<grid, 256, 0, s>>>(g);
+  }
+  if (bf16) dispatch_grouped<__nv_bfloat16>(g, transpose, b2d, sr, f46, s);
+  else dispatch_grouped<float>(g, transpose, b2d, sr, f46, s);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_quantize(const QuantArgs& a, bool bf16, bool transpose, bool b2d, bool sr, bool f46, bool rht,

@@ -20,6 +20,24 @@ struct QuantArgs {
   uint64_t seed, offset, rht_seed;
 };
 
+// Up to kQuantGroups tensors quantized by one amax launch and one encode
+// launch (the MoE experts): per group its own args and tensor amax.
+constexpr int kQuantGroups = 64;
+struct GroupQuant {
+  QuantArgs a[kQuantGroups];
+  uint32_t tiles_x[kQuantGroups];         // encoder tile-grid width per group
+  uint32_t tile_start[kQuantGroups + 1];  // encoder tiles, prefix sums
+  uint32_t amax_rows[kQuantGroups];       // amax pass: input rows per tile
+  uint32_t amax_start[kQuantGroups + 1];  // amax tiles, prefix sums
+  int count;
+};
+
+// Fills the tile tables of g (count and a[] set by the caller), then
+// launches: zero the amax accumulators and reduce every group's amax (when
+// compute_amax), and the encoder over all groups' tiles.
+cudaError_t launch_quantize_grouped(GroupQuant& g, bool bf16, bool transpose, bool b2d, bool sr, bool f46,
+                                    bool compute_amax, cudaStream_t s);
+
 cudaError_t launch_amax(const void* x, bool bf16, int64_t rows, int64_t cols, int64_t ld, float* amax_accum,
                         cudaStream_t s);
 cudaError_t launch_quantize(const QuantArgs& a, bool bf16, bool transpose, bool b2d, bool sr, bool f46, bool rht,

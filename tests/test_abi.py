@@ -28,7 +28,8 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for required in ["nvfp4_quantize", "nvfp4_rht_quantize", "nvfp4_dequantize", "nvfp4_transpose_2d", "nvfp4_gemm",
+    for required in ["nvfp4_quantize", "nvfp4_quantize_grouped", "nvfp4_rht_quantize", "nvfp4_dequantize",
+                     "nvfp4_transpose_2d", "nvfp4_gemm",
                      "nvfp4_gemm_grouped", "nvfp4_codes_bytes", "nvfp4_scales_bytes", "nvfp4_sync_check",
                      "nvfp4_status_string", "nvfp4_last_error"]:
         assert required in names
@@ -102,6 +103,20 @@ def test_gemm_argument_errors(L):
     assert L.nvfp4_gemm(ctypes.byref(A), ctypes.byref(B), D, 9, 256, None) == 1
     assert L.nvfp4_gemm_grouped(nv.MAX_GROUPS + 1, None, None, None, nv.BF16, None) == 1
     assert L.nvfp4_gemm_grouped(0, None, None, None, nv.BF16, None) == 0
+
+
+def test_quantize_grouped_argument_errors(L):
+    cfg = nv.CQuantConfig(nv.BLOCK_1D, nv.ROUND_RNE, nv.SCALE_MAX6, 0, 0, 0)
+    n = 2
+    X = (ctypes.c_void_p * n)(0x1000, 0x2000)
+    R = (ctypes.c_int64 * n)(64, 64)
+    C = (ctypes.c_int64 * n)(64, 40)
+    O = (nv.CTensor * n)(_fake_tensor(64, 64), _fake_tensor(64, 40, base=0x800000))
+    assert L.nvfp4_quantize_grouped(nv.MAX_GROUPS + 1, X, nv.BF16, R, C, C, ctypes.byref(cfg), O, None) == 1
+    assert L.nvfp4_quantize_grouped(0, None, nv.BF16, None, None, None, ctypes.byref(cfg), None, None) == 0
+    assert L.nvfp4_quantize_grouped(n, None, nv.BF16, R, C, C, ctypes.byref(cfg), O, None) == 1
+    assert L.nvfp4_quantize_grouped(n, X, nv.BF16, R, C, C, ctypes.byref(cfg), O, None) == 2   # group 1: K % 16
+    assert "group 1" in L.nvfp4_last_error().decode()
 
 
 def test_transpose_2d_argument_errors(L):
