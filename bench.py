@@ -208,6 +208,18 @@ class ClockSampler:
         return out
 
 
+def max_over_ranks(values, world: int) -> list:
+    """Element-wise max of per-rank floats over all ranks (one all-reduce;
+    on the GPU for NCCL, on the CPU for gloo)."""
+    dev = "cpu"
+    if world > 1 and torch.distributed.get_backend() == "nccl":
+        dev = torch.device("cuda", torch.cuda.current_device())
+    t = torch.tensor(list(values), dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(v) for v in t.cpu()]
+
+
 def encode_rates(nv, x, w, dev, reps=24):
     """Encode kernels alone (tensor amax supplied), back to back over copies
     whose total exceeds L2, replayed from a CUDA graph: microseconds per
@@ -343,10 +355,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize(dev)
     e2e_s = (time.perf_counter() - t0) / e2e_steps
 
-    stats = torch.tensor([step_ms, e2e_s], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(stats, op=torch.distributed.ReduceOp.MAX)
-    step_ms, e2e_s = float(stats[0]), float(stats[1])
+    step_ms, e2e_s = max_over_ranks([step_ms, e2e_s], world)
     if rank != 0:
         return None
 
@@ -526,10 +535,7 @@ def run_moe(args, rank, world, local_rank):
             d_h[e].copy_(d[e], non_blocking=True)
     torch.cuda.synchronize(dev)
     e2e_s = (time.perf_counter() - t0) / e2e_steps
-    stats = torch.tensor([step_ms, e2e_s], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(stats, op=torch.distributed.ReduceOp.MAX)
-    step_ms, e2e_s = float(stats[0]), float(stats[1])
+    step_ms, e2e_s = max_over_ranks([step_ms, e2e_s], world)
     if rank != 0:
         return None
     pk, pk_src = peaks()

@@ -123,6 +123,18 @@ nvfp4_status nvfp4_quantize(const void* x, nvfp4_dtype xt, int64_t rows, int64_t
                             void* stream);
 
 /*
+ * nvfp4_amax - the tensor amax alone (step one of the encoder): max |x| over
+ * the first `cols` columns of every row, written to the device float `amax`.
+ * For a tensor sharded across processes the caller all-reduces (MAX) the
+ * shards' amax and passes the result as amax_in to nvfp4_quantize, so every
+ * shard encodes with the global g and the shards' codes and scales equal
+ * the rows of the unsharded tensor's.  Empty tensors give 0.  x as in
+ * nvfp4_quantize (16-byte aligned, ld*elsize % 16 == 0); cols*elsize % 16 == 0.
+ */
+nvfp4_status nvfp4_amax(const void* x, nvfp4_dtype xt, int64_t rows, int64_t cols, int64_t ld, float* amax,
+                        void* stream);
+
+/*
  * nvfp4_quantize_grouped - `count` tensors quantized with one configuration
  * in one amax launch and one encode launch (per 64 tensors): the per-expert
  * tensors of a Mixture-of-Experts layer, each its own tensor with its own

@@ -69,6 +69,7 @@ def lib() -> ctypes.CDLL:
                                          ctypes.POINTER(CTensor), P, P]
         L.nvfp4_dequantize.argtypes = [ctypes.POINTER(CTensor), P, ctypes.c_int, P]
         L.nvfp4_transpose_2d.argtypes = [ctypes.POINTER(CTensor), ctypes.POINTER(CTensor), P]
+        L.nvfp4_amax.argtypes = [P, ctypes.c_int, I64, I64, I64, P, P]
         L.nvfp4_quantize_grouped.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_void_p), ctypes.c_int,
                                              ctypes.POINTER(I64), ctypes.POINTER(I64), ctypes.POINTER(I64),
                                              ctypes.POINTER(CQuantConfig), ctypes.POINTER(CTensor), P]
@@ -76,7 +77,7 @@ def lib() -> ctypes.CDLL:
         L.nvfp4_gemm_grouped.argtypes = [ctypes.c_int, ctypes.POINTER(CTensor), ctypes.POINTER(CTensor),
                                          ctypes.POINTER(ctypes.c_void_p), ctypes.c_int, P]
         L.nvfp4_sync_check.argtypes = [P]
-        for fn in ("nvfp4_quantize", "nvfp4_quantize_grouped", "nvfp4_rht_quantize", "nvfp4_dequantize",
+        for fn in ("nvfp4_amax", "nvfp4_quantize", "nvfp4_quantize_grouped", "nvfp4_rht_quantize", "nvfp4_dequantize",
                    "nvfp4_transpose_2d", "nvfp4_gemm", "nvfp4_gemm_grouped", "nvfp4_sync_check"):
             getattr(L, fn).restype = ctypes.c_int
         L.nvfp4_status_string.argtypes = [ctypes.c_int]
@@ -157,6 +158,15 @@ def _prep_input(x: torch.Tensor):
     if x.stride(1) != 1:
         raise ValueError("x must have unit column stride")
     return x.shape[0], x.shape[1], x.stride(0)
+
+
+def amax(x: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """nvfp4_amax: max |x| as a device float32 [1]."""
+    rows, cols, ld = _prep_input(x)
+    if out is None:
+        out = torch.empty(1, dtype=torch.float32, device=x.device)
+    _check(lib().nvfp4_amax(_ptr(x), _dtype_code(x.dtype), rows, cols, ld, _ptr(out), _stream(stream)), "nvfp4_amax")
+    return out
 
 
 def quantize(x: torch.Tensor, *, block="1d", rounding="rne", scaling="max6", transpose=False, seed=0, offset=0,

@@ -168,6 +168,26 @@ nvfp4_status nvfp4_rht_quantize(const void* x, nvfp4_dtype xt, int64_t rows, int
   return run_quantize(x, xt, rows, cols, ld, cfg, true, rht_seed, amax_in, out, transformed_debug, stream);
 }
 
+nvfp4_status nvfp4_amax(const void* x, nvfp4_dtype xt, int64_t rows, int64_t cols, int64_t ld, float* amax,
+                        void* stream) {
+  if (xt != NVFP4_F32 && xt != NVFP4_BF16) return fail(NVFP4_ERR_INVALID_ARG, "input dtype must be F32 or BF16");
+  if (rows < 0 || cols < 0) return fail(NVFP4_ERR_INVALID_ARG, "negative size");
+  if (ld < cols) return fail(NVFP4_ERR_INVALID_ARG, "ld < cols");
+  if (!amax) return fail(NVFP4_ERR_INVALID_ARG, "amax is NULL");
+  const int64_t es = xt == NVFP4_BF16 ? 2 : 4;
+  if (rows > 0 && cols > 0) {
+    if (!x) return fail(NVFP4_ERR_INVALID_ARG, "x is NULL");
+    if (!aligned16(x) || (ld * es) % 16 || (cols * es) % 16)
+      return fail(NVFP4_ERR_MISALIGNED, "x must be 16-byte aligned with ld*elsize and cols*elsize % 16 == 0");
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(float), s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(amax)");
+  if (rows == 0 || cols == 0) return NVFP4_OK;
+  e = nvfp4::launch_amax(x, xt == NVFP4_BF16, rows, cols, ld, amax, s);
+  return e == cudaSuccess ? NVFP4_OK : cuda_fail(e, "amax launch");
+}
+
 nvfp4_status nvfp4_quantize_grouped(int count, const void* const* x, nvfp4_dtype xt, const int64_t* rows,
                                     const int64_t* cols, const int64_t* ld, const nvfp4_quant_config* cfg,
                                     nvfp4_tensor* out, void* stream) {

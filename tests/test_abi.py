@@ -28,7 +28,7 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for required in ["nvfp4_quantize", "nvfp4_quantize_grouped", "nvfp4_rht_quantize", "nvfp4_dequantize",
+    for required in ["nvfp4_amax", "nvfp4_quantize", "nvfp4_quantize_grouped", "nvfp4_rht_quantize", "nvfp4_dequantize",
                      "nvfp4_transpose_2d", "nvfp4_gemm",
                      "nvfp4_gemm_grouped", "nvfp4_codes_bytes", "nvfp4_scales_bytes", "nvfp4_sync_check",
                      "nvfp4_status_string", "nvfp4_last_error"]:
@@ -103,6 +103,15 @@ def test_gemm_argument_errors(L):
     assert L.nvfp4_gemm(ctypes.byref(A), ctypes.byref(B), D, 9, 256, None) == 1
     assert L.nvfp4_gemm_grouped(nv.MAX_GROUPS + 1, None, None, None, nv.BF16, None) == 1
     assert L.nvfp4_gemm_grouped(0, None, None, None, nv.BF16, None) == 0
+
+
+def test_amax_argument_errors(L):
+    a = ctypes.c_void_p(0x4000)
+    assert L.nvfp4_amax(ctypes.c_void_p(0x1000), 7, 4, 64, 64, a, None) == 1          # dtype
+    assert L.nvfp4_amax(ctypes.c_void_p(0x1000), nv.BF16, 4, 64, 32, a, None) == 1    # ld < cols
+    assert L.nvfp4_amax(ctypes.c_void_p(0x1000), nv.BF16, 4, 64, 64, None, None) == 1  # amax NULL
+    assert L.nvfp4_amax(ctypes.c_void_p(0x1008), nv.BF16, 4, 64, 64, a, None) == 3    # misaligned x
+    assert L.nvfp4_amax(ctypes.c_void_p(0x1000), nv.BF16, 4, 12, 64, a, None) == 3    # cols*2 % 16
 
 
 def test_quantize_grouped_argument_errors(L):
