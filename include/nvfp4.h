@@ -213,6 +213,19 @@ nvfp4_status nvfp4_gemm(const nvfp4_tensor* A, const nvfp4_tensor* B, void* D, n
                         void* stream);
 
 /*
+ * nvfp4_gemm_amax - nvfp4_gemm that also reduces the tensor amax of its own
+ * output in the epilogue: *amax_out = max |D| over the stored values (after
+ * the BF16 rounding when dt = BF16).  The next layer's quantization of D then
+ * takes amax_out as its amax_in and skips its own amax pass over D (one read
+ * of D saved): nvfp4_quantize(D, ..., amax_in = amax_out) equals
+ * nvfp4_quantize(D, ..., amax_in = NULL) bit for bit.  amax_out: device
+ * float, zeroed and written by the call (on `stream`).  Other arguments and
+ * rules as nvfp4_gemm.
+ */
+nvfp4_status nvfp4_gemm_amax(const nvfp4_tensor* A, const nvfp4_tensor* B, void* D, nvfp4_dtype dt, int64_t ldd,
+                             float* amax_out, void* stream);
+
+/*
  * nvfp4_gemm_grouped - `count` independent GEMMs D[e] = A[e] * B[e]^T in one
  * launch (routed experts).  A, B: host arrays of `count` tensors; D: host
  * array of `count` device pointers, each row-major [M_e][N_e] (ldd = N_e).

@@ -74,11 +74,12 @@ def lib() -> ctypes.CDLL:
                                              ctypes.POINTER(I64), ctypes.POINTER(I64), ctypes.POINTER(I64),
                                              ctypes.POINTER(CQuantConfig), ctypes.POINTER(CTensor), P]
         L.nvfp4_gemm.argtypes = [ctypes.POINTER(CTensor), ctypes.POINTER(CTensor), P, ctypes.c_int, I64, P]
+        L.nvfp4_gemm_amax.argtypes = [ctypes.POINTER(CTensor), ctypes.POINTER(CTensor), P, ctypes.c_int, I64, P, P]
         L.nvfp4_gemm_grouped.argtypes = [ctypes.c_int, ctypes.POINTER(CTensor), ctypes.POINTER(CTensor),
                                          ctypes.POINTER(ctypes.c_void_p), ctypes.c_int, P]
         L.nvfp4_sync_check.argtypes = [P]
         for fn in ("nvfp4_amax", "nvfp4_quantize", "nvfp4_quantize_grouped", "nvfp4_rht_quantize", "nvfp4_dequantize",
-                   "nvfp4_transpose_2d", "nvfp4_gemm", "nvfp4_gemm_grouped", "nvfp4_sync_check"):
+                   "nvfp4_transpose_2d", "nvfp4_gemm", "nvfp4_gemm_amax", "nvfp4_gemm_grouped", "nvfp4_sync_check"):
             getattr(L, fn).restype = ctypes.c_int
         L.nvfp4_status_string.argtypes = [ctypes.c_int]
         L.nvfp4_status_string.restype = ctypes.c_char_p
@@ -253,6 +254,20 @@ def gemm(a: NVFP4Tensor, b: NVFP4Tensor, out_dtype=torch.bfloat16, out: torch.Te
     _check(lib().nvfp4_gemm(ctypes.byref(ca), ctypes.byref(cb), _ptr(out), _dtype_code(out.dtype), out.stride(0),
                             _stream(stream)), "nvfp4_gemm")
     return out
+
+
+def gemm_amax(a: NVFP4Tensor, b: NVFP4Tensor, out_dtype=torch.bfloat16, out: torch.Tensor | None = None,
+              amax_out: torch.Tensor | None = None, stream=None):
+    """nvfp4_gemm_amax: D as nvfp4_gemm plus max |D| (as stored) reduced in the
+    GEMM epilogue.  Returns (D, amax float32 [1])."""
+    if out is None:
+        out = torch.empty((a.rows, b.rows), dtype=out_dtype, device=a.codes.device)
+    if amax_out is None:
+        amax_out = torch.empty(1, dtype=torch.float32, device=a.codes.device)
+    ca, cb = a.c(), b.c()
+    _check(lib().nvfp4_gemm_amax(ctypes.byref(ca), ctypes.byref(cb), _ptr(out), _dtype_code(out.dtype), out.stride(0),
+                                 _ptr(amax_out), _stream(stream)), "nvfp4_gemm_amax")
+    return out, amax_out
 
 
 def gemm_grouped(a: list, b: list, out_dtype=torch.bfloat16, out: list | None = None, stream=None) -> list:

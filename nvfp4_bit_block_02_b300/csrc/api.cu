@@ -272,8 +272,9 @@ nvfp4_status nvfp4_dequantize(const nvfp4_tensor* q, void* y, nvfp4_dtype yt, vo
   return e == cudaSuccess ? NVFP4_OK : cuda_fail(e, "dequantize launch");
 }
 
-nvfp4_status nvfp4_gemm(const nvfp4_tensor* A, const nvfp4_tensor* B, void* D, nvfp4_dtype dt, int64_t ldd,
-                        void* stream) {
+namespace {
+nvfp4_status run_gemm(const nvfp4_tensor* A, const nvfp4_tensor* B, void* D, nvfp4_dtype dt, int64_t ldd,
+                      float* amax_out, void* stream) {
   nvfp4_status st = check_gemm_operands(A, B);
   if (st != NVFP4_OK) return st;
   if (dt != NVFP4_F32 && dt != NVFP4_BF16) return fail(NVFP4_ERR_INVALID_ARG, "output dtype must be F32 or BF16");
@@ -284,9 +285,27 @@ nvfp4_status nvfp4_gemm(const nvfp4_tensor* A, const nvfp4_tensor* B, void* D, n
   if (!aligned16(D) || (ldd * es) % 16) return fail(NVFP4_ERR_MISALIGNED, "D must be 16-byte aligned, ldd*elsize % 16 == 0");
   const char* why = "";
   cudaError_t e = nvfp4::launch_gemm(operand(A), operand(B), D, ldd, dt == NVFP4_BF16,
-                                     reinterpret_cast<cudaStream_t>(stream), &why);
+                                     reinterpret_cast<cudaStream_t>(stream), &why, amax_out);
   if (e != cudaSuccess) return cuda_fail(e, (std::string("gemm launch: ") + why).c_str());
   return NVFP4_OK;
+}
+}  // namespace
+
+nvfp4_status nvfp4_gemm(const nvfp4_tensor* A, const nvfp4_tensor* B, void* D, nvfp4_dtype dt, int64_t ldd,
+                        void* stream) {
+  return run_gemm(A, B, D, dt, ldd, nullptr, stream);
+}
+
+nvfp4_status nvfp4_gemm_amax(const nvfp4_tensor* A, const nvfp4_tensor* B, void* D, nvfp4_dtype dt, int64_t ldd,
+                             float* amax_out, void* stream) {
+  if (!amax_out) return fail(NVFP4_ERR_INVALID_ARG, "amax_out is NULL");
+  if (!A || !B) return fail(NVFP4_ERR_INVALID_ARG, "A or B is NULL");
+  // arguments first (nothing launched on error), then zero the accumulator
+  nvfp4_status st = check_gemm_operands(A, B);
+  if (st != NVFP4_OK) return st;
+  cudaError_t e = cudaMemsetAsync(amax_out, 0, sizeof(float), reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(amax_out)");
+  return run_gemm(A, B, D, dt, ldd, amax_out, stream);
 }
 
 nvfp4_status nvfp4_gemm_grouped(int count, const nvfp4_tensor* A, const nvfp4_tensor* B, void* const* D,

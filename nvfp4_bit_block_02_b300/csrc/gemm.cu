@@ -335,7 +335,8 @@ struct GroupedSched {
 };
 
 template <class Sched>
-__device__ __forceinline__ void gemm_pairs(const Sched& sched, bool out_bf16, unsigned int* err) {
+__device__ __forceinline__ void gemm_pairs(const Sched& sched, bool out_bf16, unsigned int* err,
+                                           unsigned int* amax_out) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
@@ -575,6 +576,16 @@ __device__ __forceinline__ void gemm_pairs(const Sched& sched, bool out_bf16, un
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(lead_accum_empty);
+        if (amax_out && active) {
+          // producer amax of the stored BF16 values: |x| bit patterns order
+          // like unsigned integers, two per word
+          uint32_t mx = 0;
+#pragma unroll
+          for (int i = 0; i < 64; ++i) mx = __vmaxu2(mx, pk[i] & 0x7FFF7FFFu);
+          uint32_t m = max(mx & 0xFFFFu, mx >> 16) << 16;
+          m = __reduce_max_sync(0xFFFFFFFFu, m);
+          if (lane == 0 && m) atomicMax(amax_out, m);
+        }
         if (active) {
 #pragma unroll
           for (int cc = 0; cc < 2; ++cc) {  // 64 columns = one 128-byte box row
@@ -605,6 +616,14 @@ __device__ __forceinline__ void gemm_pairs(const Sched& sched, bool out_bf16, un
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(lead_accum_empty);
+          }
+          if (amax_out && active) {
+            uint32_t m = 0;
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              m = max(m, __float_as_uint(__fmul_rn(alpha, __uint_as_float(r[i]))) & 0x7FFFFFFFu);
+            m = __reduce_max_sync(0xFFFFFFFFu, m);
+            if (lane == 0 && m) atomicMax(amax_out, m);
           }
           if (active) {
             if (lane == 0) bulk_wait_read0();
@@ -642,12 +661,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
            const __grid_constant__ CUtensorMap tmD, const __grid_constant__ GemmArgs a) {
   SingleSched s{&tmA, &tmB, &tmD, &a};
-  gemm_pairs(s, a.out_bf16 != 0, a.err);
+  gemm_pairs(s, a.out_bf16 != 0, a.err, a.amax_out);
 }
 
 __global__ void __launch_bounds__(NUM_THREADS, 1) k_gemm_grouped(const __grid_constant__ GroupedArgs g) {
   GroupedSched s{&g};
-  gemm_pairs(s, g.out_bf16 != 0, g.err);
+  gemm_pairs(s, g.out_bf16 != 0, g.err, nullptr);
 }
 
 // ---------------------------------------------------------------------------
@@ -754,7 +773,7 @@ int gemm_tile_m() { return 2 * BM; }
 int gemm_tile_n() { return BN; }
 
 cudaError_t launch_gemm(const GemmOperand& A, const GemmOperand& B, void* D, int64_t ldd, bool out_bf16, cudaStream_t s,
-                        const char** why) {
+                        const char** why, float* amax_out) {
   CUtensorMap ta, tb, td;
   if (!make_code_map(&ta, A.codes, A.rows, A.K) || !make_code_map(&tb, B.codes, B.rows, B.K) ||
       !make_out_map(&td, D, A.rows, B.rows, ldd, out_bf16)) {
@@ -774,7 +793,8 @@ cudaError_t launch_gemm(const GemmOperand& A, const GemmOperand& B, void* D, int
     }
     cfg = true;
   }
-  GemmArgs a{A.scales, B.scales, A.g, B.g, (int)A.rows, (int)B.rows, (int)A.K, out_bf16 ? 1 : 0, err};
+  GemmArgs a{A.scales, B.scales, A.g, B.g, (int)A.rows, (int)B.rows, (int)A.K, out_bf16 ? 1 : 0, err,
+             reinterpret_cast<unsigned int*>(amax_out)};
   const int tiles = (int)((A.rows + 2 * BM - 1) / (2 * BM)) * (int)((B.rows + BN - 1) / BN);
   static int max_pairs = 0;
   cudaError_t e = launch_pairs(k_gemm, tiles, &max_pairs, s, ta, tb, td, a);

@@ -22,6 +22,7 @@ struct GemmArgs {
   int M, N, K;
   int out_bf16;
   unsigned int* err;
+  unsigned int* amax_out;  // nullable: atomicMax of |D| (as stored) over the output, float bits
 };
 
 constexpr int kGroupsPerLaunch = 64;
@@ -45,7 +46,7 @@ unsigned int* device_error_word();
 int gemm_tile_m();
 int gemm_tile_n();
 cudaError_t launch_gemm(const GemmOperand& A, const GemmOperand& B, void* D, int64_t ldd, bool out_bf16, cudaStream_t s,
-                        const char** why);
+                        const char** why, float* amax_out = nullptr);
 cudaError_t launch_gemm_grouped(int count, const GemmOperand* A, const GemmOperand* B, void* const* D, bool out_bf16,
                                 cudaStream_t s, const char** why);
 

@@ -29,7 +29,7 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for required in ["nvfp4_amax", "nvfp4_quantize", "nvfp4_quantize_grouped", "nvfp4_rht_quantize", "nvfp4_dequantize",
-                     "nvfp4_transpose_2d", "nvfp4_gemm",
+                     "nvfp4_transpose_2d", "nvfp4_gemm", "nvfp4_gemm_amax",
                      "nvfp4_gemm_grouped", "nvfp4_codes_bytes", "nvfp4_scales_bytes", "nvfp4_sync_check",
                      "nvfp4_status_string", "nvfp4_last_error"]:
         assert required in names
@@ -156,3 +156,12 @@ def test_empty_tensors_are_ok_without_launch_for_gemm(L):
     A = _fake_tensor(0, 256)
     B = _fake_tensor(128, 256)
     assert L.nvfp4_gemm(ctypes.byref(A), ctypes.byref(B), ctypes.c_void_p(0x4000000), nv.BF16, 128, None) == 0
+
+
+def test_gemm_amax_argument_errors(L):
+    A = _fake_tensor(128, 256)
+    B = _fake_tensor(256, 256, base=0x800000)
+    D = ctypes.c_void_p(0x4000000)
+    assert L.nvfp4_gemm_amax(ctypes.byref(A), ctypes.byref(B), D, nv.BF16, 256, None, None) == 1   # amax_out NULL
+    assert L.nvfp4_gemm_amax(ctypes.byref(A), ctypes.byref(_fake_tensor(256, 512)), D, nv.BF16, 256,
+                             ctypes.c_void_p(0x5000000), None) == 1                                  # K differs
