@@ -32,8 +32,13 @@ METRIC = "quantize HBM GB/s and NVFP4 GEMM TFLOPS, each as % of B300 roofline"
 FP4_OVER_BF16 = 13.5 / 2.25          # nominal dense FP4 : BF16 tensor ratio of B300
 FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
-# workload name -> (M, N, K, X dtype, builder, description)
+# workload name -> GEMM shape and description (the step of each is built in make_plan)
 WORKLOADS = {
+    "pr1": dict(M=256, N=256, K=256, desc="PR1: A, B 256x256 f32 N(0,1) with 1% of entries x50 (seeds 0, 1), "
+                                         "1D RNE max-6, GEMM 256x256x256 FP32 out"),
+    "wgrad": dict(M=14336, N=4096, K=8192, desc="Llama-3-8B MLP wgrad: dY 8192x14336 bf16 1e-3*t(4) (RHT along the "
+                                               "tokens + SR seed 1, transposed), X 8192x4096 bf16 (RHT, transposed), "
+                                               "rht_seed 1, GEMM 14336x4096x8192 FP32 out"),
     "llama8b": dict(M=8192, N=14336, K=4096, desc="Llama-3-8B MLP fprop: X 8192x4096 bf16 N(0,1) + 0.1% channels x20 "
                                                  "(1D, RNE, max-6), W 14336x4096 bf16 N(0,0.02) (2D 16x16), "
                                                  "GEMM 8192x14336x4096 BF16 out"),
@@ -258,6 +263,43 @@ def encode_rates(nv, x, w, dev, reps=24):
 # --------------------------------------------------------------------------
 # our implementation
 # --------------------------------------------------------------------------
+def make_plan(workload: str, nv, synthetic, dev):
+    """The step of a workload: its host inputs, device inputs, components
+    (name, call, elements quantized, input bytes per element) with the GEMM
+    last, the output D and the launches of our kernels per step."""
+    c = WORKLOADS[workload]
+    M, N, K = c["M"], c["N"], c["K"]
+    if workload == "pr1":
+        wl = synthetic.pr1()
+        a_h, b_h = wl.tensors["A"], wl.tensors["B"]
+    elif workload == "wgrad":
+        wl = synthetic.wgrad()
+        a_h, b_h = wl.tensors["dY"], wl.tensors["X"]
+    else:
+        wl = synthetic.llama8b_fprop() if workload == "llama8b" else synthetic.llama405b_fprop()
+        a_h, b_h = wl.tensors["X"], wl.tensors["W"]
+    a_h, b_h = a_h.pin_memory(), b_h.pin_memory()
+    a, b = a_h.to(dev), b_h.to(dev)
+    qa = nv.NVFP4Tensor.empty(M, K, device=dev)
+    qb = nv.NVFP4Tensor.empty(N, K, device=dev)
+    out_dtype = torch.float32 if workload in ("pr1", "wgrad") else torch.bfloat16
+    d = torch.empty((M, N), dtype=out_dtype, device=dev)
+    es = a.element_size()
+    if workload == "wgrad":
+        parts = [("quantize_dYT_rht_sr", lambda: nv.rht_quantize(a, rht_seed=1, transpose=True, rounding="stochastic",
+                                                                 seed=1, out=qa), a.numel(), es),
+                 ("quantize_XT_rht", lambda: nv.rht_quantize(b, rht_seed=1, transpose=True, out=qb), b.numel(), es)]
+    elif workload == "pr1":
+        parts = [("quantize_A", lambda: nv.quantize(a, out=qa), a.numel(), es),
+                 ("quantize_B", lambda: nv.quantize(b, out=qb), b.numel(), es)]
+    else:
+        parts = [("quantize_X", lambda: nv.quantize(a, out=qa), a.numel(), es),
+                 ("quantize_W_2d", lambda: nv.quantize(b, block="2d", out=qb), b.numel(), es)]
+    parts.append(("gemm", lambda: nv.gemm(qa, qb, out=d), None, None))
+    # RHT: an amax-only pass of the transform and the encode; plain: amax + encode; GEMM: 1
+    return dict(inputs_h=[a_h, b_h], inputs=[a, b], parts=parts, out=d, M=M, N=N, K=K, launches=5, fwd=(a, b))
+
+
 def run_ours(args, rank, world, local_rank):
     import nvfp4_bit_block_02_b300 as nv
     import synthetic
@@ -265,25 +307,17 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     cfgw = WORKLOADS[args.workload]
-    M, N, K = cfgw["M"], cfgw["N"], cfgw["K"]
-    if args.workload == "llama8b":
-        wl = synthetic.llama8b_fprop()
-    else:
-        wl = synthetic.llama405b_fprop()
-    x_h = wl.tensors["X"].pin_memory()
-    w_h = wl.tensors["W"].pin_memory()
-    x = x_h.to(dev)
-    w = w_h.to(dev)
-    qx = nv.NVFP4Tensor.empty(M, K, device=dev)
-    qw = nv.NVFP4Tensor.empty(N, K, device=dev)
-    d = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    plan = make_plan(args.workload, nv, synthetic, dev)
+    M, N, K = plan["M"], plan["N"], plan["K"]
+    x_h, w_h = plan["inputs_h"]
+    x, w = plan["inputs"]
+    d = plan["out"]
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
-    launches_per_step = 5  # amax + encode for X and W, GEMM
+    launches_per_step = plan["launches"]
 
-    def step(stream=None):
-        nv.quantize(x, out=qx, stream=stream)
-        nv.quantize(w, block="2d", out=qw, stream=stream)
-        nv.gemm(qx, qw, out=d, stream=stream)
+    def step():
+        for _, fn, _, _ in plan["parts"]:
+            fn()
 
     # The step and each of its components are captured once as CUDA graphs
     # and replayed, so the device timeline carries no host-side launch gaps.
@@ -297,12 +331,9 @@ def run_ours(args, rank, world, local_rank):
     with torch.cuda.stream(side):
         with torch.cuda.graph(g_step, stream=side):
             step()
-        with torch.cuda.graph(parts[0], stream=side):
-            nv.quantize(x, out=qx)
-        with torch.cuda.graph(parts[1], stream=side):
-            nv.quantize(w, block="2d", out=qw)
-        with torch.cuda.graph(parts[2], stream=side):
-            nv.gemm(qx, qw, out=d)
+        for g, (_, fn, _, _) in zip(parts, plan["parts"]):
+            with torch.cuda.graph(g, stream=side):
+                fn()
     torch.cuda.current_stream(dev).wait_stream(side)
     stream = torch.cuda.current_stream(dev)
     for _ in range(args.warmup):
@@ -338,12 +369,11 @@ def run_ours(args, rank, world, local_rank):
             g.replay()
         evc[i][3].record(stream)
     torch.cuda.synchronize(dev)
-    t_qx = [evc[i][0].elapsed_time(evc[i][1]) for i in range(args.steps)]
-    t_qw = [evc[i][1].elapsed_time(evc[i][2]) for i in range(args.steps)]
-    t_gm = [evc[i][2].elapsed_time(evc[i][3]) for i in range(args.steps)]
-    enc = encode_rates(nv, x, w, dev) if rank == 0 else None
+    t_parts = [[evc[i][j].elapsed_time(evc[i][j + 1]) for i in range(args.steps)] for j in range(3)]
+    t_gm = t_parts[2]
+    enc = encode_rates(nv, x, w, dev) if rank == 0 and args.workload in ("llama8b", "llama405b") else None
     # end to end through the public API from pinned host buffers, D read back
-    d_h = torch.empty((M, N), dtype=torch.bfloat16, pin_memory=True)
+    d_h = torch.empty((M, N), dtype=d.dtype, pin_memory=True)
     e2e_steps = max(2, min(args.steps, 5))
     torch.cuda.synchronize(dev)
     t0 = time.perf_counter()
@@ -364,12 +394,19 @@ def run_ours(args, rank, world, local_rank):
     ms_per_step = step_ms / args.steps
     value = world * flops / (ms_per_step * 1e-3) / 1e12
     gemm_ms = statistics.mean(t_gm)
-    qx_ms, qw_ms = statistics.mean(t_qx), statistics.mean(t_qw)
-    # algorithmic bytes of the quantizer (BF16 in): 2 B read + 0.5 B codes + 1/16 B scales per element,
-    # plus the second read of the tensor amax pass
-    qbytes = lambda n: n * (2 + 0.5 + 1 / 16)
-    amax_bytes = lambda n: n * 2
-    fp4_peak = pk["bf16_tflops"] * FP4_OVER_BF16
+    # algorithmic bytes of the quantizer: in-bytes read + 0.5 B codes + 1/16 B scales per element, plus the
+    # second read of the tensor amax pass
+    qbytes = lambda n, es=2: n * (es + 0.5 + 1 / 16)
+    amax_bytes = lambda n, es=2: n * es
+    comps = {}
+    for j, (name, _, elems, es) in enumerate(plan["parts"][:2]):
+        ms = statistics.mean(t_parts[j])
+        comps[name] = {"ms": round(ms, 4), "GB_s": round((qbytes(elems, es) + amax_bytes(elems, es)) / (ms * 1e-3) / 1e9, 1),
+                       "bytes_per_elem": f"{es} read + 0.5625 written (encode) + {es} read (amax pass)"}
+    # a timed region that ran power-capped is a sustained regime: its denominator is the sustained peak
+    sustained = bool(clocks and "sw_power_cap" in (clocks.get("reasons") or []))
+    fp4_burst = pk["bf16_tflops"] * FP4_OVER_BF16
+    fp4_peak = (pk["bf16_tflops_sustained"] if sustained else pk["bf16_tflops"]) * FP4_OVER_BF16
     gemm_tflops = flops / (gemm_ms * 1e-3) / 1e12
     traffic = ncu_traffic("k_gemm", source_hash("gemm.cu", "gemm.h"))
     q_traffic = ncu_traffic("k_quant_rows", source_hash("quantize.cu", "nvfp4_device.cuh"))
@@ -390,17 +427,17 @@ def run_ours(args, rank, world, local_rank):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "fp4(e2m1)+e4m3 scales, fp32 accumulate; bf16 in/out",
+        "dtype": f"fp4(e2m1)+e4m3 scales, fp32 accumulate; {str(x.dtype).replace('torch.', '')} in, "
+                 f"{str(d.dtype).replace('torch.', '')} out",
         "data": "synthetic (seeded numpy draws, the pages' shapes; no model weights)",
         "config": {"workload": args.workload, "M": M, "N": N, "K": K, "desc": cfgw["desc"],
-                   "l2": "256 MiB flush write between steps (outside the timed events); inputs 176 MiB > L2",
+                   "l2": f"256 MiB flush write between steps (outside the timed events); inputs "
+                         f"{(x.numel() * x.element_size() + w.numel() * w.element_size()) / 2**20:.0f} MiB",
                    "timing": "the step (and, for the component breakdown, each component) captured once as a CUDA "
                              "graph and replayed between CUDA events on the launching stream",
-                   "value_is": "2*M*N*K / (quantize X + quantize W + GEMM) step time, summed over ranks"},
+                   "value_is": "2*M*N*K / (quantize both operands + GEMM) step time, summed over ranks"},
         "components": {
-            "quantize_X": {"ms": round(qx_ms, 4), "GB_s": round((qbytes(M * K) + amax_bytes(M * K)) / (qx_ms * 1e-3) / 1e9, 1),
-                           "encode_bytes_per_elem": 2.5625, "amax_pass_bytes_per_elem": 2.0},
-            "quantize_W_2d": {"ms": round(qw_ms, 4), "GB_s": round((qbytes(N * K) + amax_bytes(N * K)) / (qw_ms * 1e-3) / 1e9, 1)},
+            **comps,
             "gemm": {"ms": round(gemm_ms, 4), "TFLOP_s": round(gemm_tflops, 1),
                      "frac_of_fp4_peak": round(gemm_tflops / fp4_peak, 4)},
             # the encode kernel alone (tensor amax supplied), the quantizer's roofline figure
@@ -416,11 +453,15 @@ def run_ours(args, rank, world, local_rank):
         "roofline": {"bound": "tensor", "kernel": "k_gemm (tcgen05 mxf4nvf4 block-scaled)",
                      "achieved": round(gemm_tflops, 1), "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
                      "frac": round(gemm_tflops / fp4_peak, 4), "traffic": traffic,
-                     "peak_source": f"{pk_src} bf16 burst {pk['bf16_tflops']} TFLOP/s x {FP4_OVER_BF16} "
-                                    "(nominal FP4:BF16 dense ratio)"},
+                     "frac_of_burst_peak": round(gemm_tflops / fp4_burst, 4),
+                     "peak_source": (f"{pk_src} bf16 {'sustained' if sustained else 'burst'} "
+                                     f"{pk['bf16_tflops_sustained'] if sustained else pk['bf16_tflops']} TFLOP/s x "
+                                     f"{FP4_OVER_BF16} (nominal FP4:BF16 dense ratio)"
+                                     + ("; sustained because the timed region ran under sw_power_cap" if sustained
+                                        else ""))},
         "e2e": {"value": round(world * flops / e2e_s / 1e12, 3), "unit": "TFLOP/s",
-                "h2d_bytes_per_step": int(x_h.numel() * 2 + w_h.numel() * 2),
-                "d2h_bytes_per_step": int(d_h.numel() * 2)},
+                "h2d_bytes_per_step": int(x_h.numel() * x_h.element_size() + w_h.numel() * w_h.element_size()),
+                "d2h_bytes_per_step": int(d_h.numel() * d_h.element_size())},
         "gpu_launches": launches_per_step * args.steps * world,
         "clocks": clocks,
     }
@@ -592,33 +633,51 @@ def _oracle_inputs(workload: str):
         c = WORKLOADS["moe"]
         wl = synthetic.moe(1, c["M"], c["K"], c["N"])
         return wl.tensors["X"][0].to(torch.float32).numpy(), wl.tensors["W"][0].to(torch.float32).numpy()
+    if workload == "pr1":
+        wl = synthetic.pr1()
+        return wl.tensors["A"].numpy(), wl.tensors["B"].numpy()
+    if workload == "wgrad":
+        wl = synthetic.wgrad()
+        return wl.tensors["dY"].to(torch.float32).numpy(), wl.tensors["X"].to(torch.float32).numpy()
     wl = synthetic.llama8b_fprop() if workload == "llama8b" else synthetic.llama405b_fprop()
     return wl.tensors["X"].to(torch.float32).numpy(), wl.tensors["W"].to(torch.float32).numpy()
 
 
 def _oracle_sample(workload: str, X, W, rx: int, rw: int, rg: int):
-    """Time the oracle on rows [0, rx) of X, [0, rw) of W and rg GEMM output
-    rows; return the time scaled to one whole step of the workload."""
+    """Time the oracle on a slice of the step and return (time scaled to one
+    whole step, seconds spent).  Fprop-shaped workloads: rows [0, rx) of X
+    (1D), [0, rw) of W (2D), rg GEMM output rows against those rw columns.
+    Wgrad: the first rx columns of dY and rw columns of X (their transposed,
+    RHT, quantization), rg output rows.  MoE: one expert, rg output rows."""
     import oracle
     c = WORKLOADS[workload]
+    M, N = c["M"], c["N"]
     if workload == "moe":   # one expert: W^T with Four-over-Six, X max-6; scaled to E experts
-        E, M = c["E"], c["M"]
+        E, Mt = c["E"], c["M"]
         t0 = time.perf_counter()
         qw = oracle.quantize(W, transpose=True, four_over_six=True)
         qx = oracle.quantize(X)
         t1 = time.perf_counter()
         oracle.gemm_reference(qx, qw, rows=np.arange(rg))
         t2 = time.perf_counter()
-        return E * ((t1 - t0) + (t2 - t1) * M / rg), t2 - t0
-    M, N = c["M"], c["N"]
+        return E * ((t1 - t0) + (t2 - t1) * Mt / rg), t2 - t0
     t0 = time.perf_counter()
-    qx = oracle.quantize(X[:rx])
-    t1 = time.perf_counter()
-    qw = oracle.quantize(W[:rw], block2d=True)
+    if workload == "wgrad":   # output rows = columns of the inputs
+        qa = oracle.quantize(np.ascontiguousarray(X[:, :rx]), transpose=True, rht=True, stochastic=True, seed=1,
+                             rht_seed=1)
+        t1 = time.perf_counter()
+        qb = oracle.quantize(np.ascontiguousarray(W[:, :rw]), transpose=True, rht=True, rht_seed=1)
+        sa, sb = M / rx, N / rw
+    else:
+        qa = oracle.quantize(X[:rx])
+        t1 = time.perf_counter()
+        qb = oracle.quantize(W[:rw], block2d=workload != "pr1")
+        sa, sb = M / rx, N / rw
     t2 = time.perf_counter()
-    oracle.gemm_reference(qx, qw, rows=np.arange(min(rg, rx)))
+    g = min(rg, qa.R)
+    oracle.gemm_reference(qa, qb, rows=np.arange(g))
     t3 = time.perf_counter()
-    return (t1 - t0) * M / rx + (t2 - t1) * N / rw + (t3 - t2) * (M / min(rg, rx)) * (N / rw), t3 - t0
+    return (t1 - t0) * sa + (t2 - t1) * sb + (t3 - t2) * (M / g) * sb, t3 - t0
 
 
 def _flops(workload: str) -> float:
@@ -626,25 +685,25 @@ def _flops(workload: str) -> float:
     return 2.0 * c.get("E", 1) * c["M"] * c["N"] * c["K"]
 
 
+# per workload: the slice the oracle is timed on (see _oracle_sample), as (rx, rw, rg)
+_CPU_SAMPLE = {"pr1": (256, 256, 256), "llama8b": (8192, 14336, 2048), "llama405b": (2048, 4096, 256),
+               "wgrad": (2048, 1024, 512), "moe": (0, 0, 256)}
+_REF_SAMPLE = {"pr1": (256, 256, 64), "llama8b": (512, 896, 64), "llama405b": (128, 256, 16),
+               "wgrad": (256, 64, 64), "moe": (0, 0, 16)}
+
+
 def cpu_baseline(workload: str):
     """The oracle as it stands on the host cores, on a bounded sample of one
-    step (a few seconds of CPU work): all of X and W quantized and 2048
-    output rows of the fp64 GEMM (MoE: one expert, 256 rows), scaled to the
-    whole step."""
+    step (a few seconds of CPU work), scaled to the whole step."""
     import oracle
     oracle.build()
     X, W = _oracle_inputs(workload)
-    if workload == "moe":
-        rx = rw = 0
-        rg = 256
-        sample = "oracle on expert 0: W_0^T Four-over-Six and X_0 quantized, fp64 GEMM of 256 rows; scaled to 64 experts"
-    else:
-        rx, rw, rg = X.shape[0], W.shape[0], 2048
-        sample = (f"oracle quantize of all of X ({X.shape[0]} rows, 1D) and W ({W.shape[0]} rows, 2D), fp64 GEMM "
-                  f"of {rg} output rows; GEMM time scaled to all rows")
+    rx, rw, rg = _CPU_SAMPLE[workload]
     t_step, spent = _oracle_sample(workload, X, W, rx, rw, rg)
     return {"value": round(_flops(workload) / t_step / 1e12, 6), "unit": "TFLOP/s",
-            "cores": len(os.sched_getaffinity(0)), "kind": "oracle", "sample": sample,
+            "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+            "sample": f"{workload}: oracle quantize of a slice (rx={rx}, rw={rw}) and fp64 GEMM of {rg} output rows, "
+                      "each part scaled to the whole step (MoE: one expert, scaled to 64)",
             "sample_seconds": round(spent, 2), "extrapolated_step_seconds": round(t_step, 2)}
 
 
@@ -655,14 +714,9 @@ def run_reference(args):
     import oracle
     oracle.build()
     X, W = _oracle_inputs(args.workload)
-    if args.workload == "moe":
-        rx = rw = 0
-        rg = 16
-        sample = "per step: oracle on expert 0 (W_0^T Four-over-Six, X_0 max-6, fp64 GEMM of 16 rows), scaled to 64 experts"
-    else:
-        rx, rw, rg = 512, 896, 64
-        sample = (f"per step: oracle quantize of X[:{rx}] (1D) and W[:{rw}] (2D), fp64 GEMM of {rg} rows; "
-                  f"scaled to the whole step")
+    rx, rw, rg = _REF_SAMPLE[args.workload]
+    sample = (f"per step: {args.workload} oracle quantize of a slice (rx={rx}, rw={rw}) and fp64 GEMM of {rg} "
+              "output rows, each part scaled to the whole step (MoE: one expert, scaled to 64)")
     for _ in range(args.warmup):
         _oracle_sample(args.workload, X, W, rx, rw, rg)
     t_steps = [_oracle_sample(args.workload, X, W, rx, rw, rg)[0] for _ in range(max(1, args.steps))]
