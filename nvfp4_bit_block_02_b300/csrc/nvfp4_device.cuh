@@ -8,6 +8,7 @@
 #pragma once
 #include <cstdint>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 namespace nvfp4 {
@@ -205,16 +206,26 @@ __device__ __forceinline__ uint2 encode16(const float v[16], float rcp, const ui
   }
 }
 
+// The two E2M1 codes of byte `b` (low nibble first) -> their values in fp32,
+// exact (every E2M1 value is an f16): one hardware conversion per pair.
+__device__ __forceinline__ float2 e2m1x2_values(uint32_t b) {
+  uint32_t h;
+  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(h) : "r"(b));
+  return __half22float2(*reinterpret_cast<const __half2*>(&h));
+}
+
 // Squared error of 16 encoded values against their decode fl(fl(v*s)*g),
-// pairwise summed: ((e0+e1)+(e2+e3)) + ... over the 16 in order.
+// pairwise summed: ((e0+e1)+(e2+e3)) + ... over the 16 in order.  Scalar
+// IEEE operations throughout; the codes are decoded two at a time.
 __device__ __forceinline__ float block_sq_err16(const float v[16], uint2 codes, float s, float g) {
   float e[16];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    uint32_t c = ((i < 8 ? codes.x : codes.y) >> (4 * (i & 7))) & 15u;
-    float deq = __fmul_rn(__fmul_rn(e2m1_value(c), s), g);
-    float d = __fsub_rn(v[i], deq);
-    e[i] = __fmul_rn(d, d);
+  for (int j = 0; j < 8; ++j) {
+    const float2 val = e2m1x2_values((j < 4 ? codes.x : codes.y) >> (8 * (j & 3)));
+    const float d0 = __fsub_rn(v[2 * j], __fmul_rn(__fmul_rn(val.x, s), g));
+    const float d1 = __fsub_rn(v[2 * j + 1], __fmul_rn(__fmul_rn(val.y, s), g));
+    e[2 * j] = __fmul_rn(d0, d0);
+    e[2 * j + 1] = __fmul_rn(d1, d1);
   }
 #pragma unroll
   for (int w = 1; w < 16; w <<= 1) {
