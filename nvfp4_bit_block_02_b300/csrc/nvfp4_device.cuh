@@ -40,10 +40,12 @@ __device__ __forceinline__ uint32_t e4m3_rne_sat(float t) {
   return r & 0xFFu;
 }
 
-// E4M3 byte (sign clear, not NaN) -> fp32, exact.
+// E4M3 byte (sign clear, not NaN) -> fp32, exact: the hardware conversion to
+// f16 (every E4M3 value is an f16), then to f32.
 __device__ __forceinline__ float e4m3_value(uint32_t b) {
-  uint32_t e = (b >> 3) & 15u, m = b & 7u;
-  return e ? __uint_as_float(((e + 120u) << 23) | (m << 20)) : __fmul_rn((float)m, 0.001953125f);
+  uint32_t h;
+  asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(h) : "r"(b & 0xFFu));
+  return __low2float(*reinterpret_cast<const __half2*>(&h));
 }
 
 // Magnitude of E2M1 index m (0..7): 0, .5, 1, 1.5, 2, 3, 4, 6 (exact bits).
