@@ -236,6 +236,25 @@ def exact_values(codes: np.ndarray, scales: np.ndarray, g: float) -> np.ndarray:
     return E2M1_VALUES[c] * s * np.float64(g)
 
 
+def bf16_round(x: np.ndarray) -> np.ndarray:
+    """fp32 -> nearest BF16 value (ties to even), returned as fp32: keep the
+    top 16 bits after adding 0x7FFF plus the lowest kept bit (finite inputs)."""
+    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    r = ((b + 0x7FFF + ((b >> 16) & 1)) & 0xFFFF0000).astype(np.uint32)
+    return r.view(np.float32)
+
+
+def w4a16_reference(x: np.ndarray, qw: Quantized, rows=None):
+    """Y = X @ W_hat^T in float64 and the bound sum_k |x||w_hat|: the weight-only
+    path, where the NVFP4 weight enters a BF16 GEMM as W_hat = BF16(decode),
+    decode = fl(fl(value(code) * s_b) * g) (``dequantize``), rounded to the
+    nearest BF16 (ties to even).  ``x``: the fp32 values of the BF16
+    activations, M x K; ``qw``: N x K."""
+    w = bf16_round(dequantize(qw.codes, qw.scales, qw.g)).astype(np.float64)
+    a = np.asarray(x if rows is None else x[rows], dtype=np.float64)
+    return a @ w.T, np.abs(a) @ np.abs(w).T
+
+
 def gemm_reference(qa: Quantized, qb: Quantized, rows=None):
     """D = A_deq @ B_deq^T in float64 and the bound sum_k |a||b|.
 

@@ -2,7 +2,9 @@
 representable products checked in integer arithmetic, and the closed form
 of an all-ones product."""
 import numpy as np
+import torch
 
+import oracle
 from synthetic import normal
 
 
@@ -71,3 +73,44 @@ def test_gemm_brute_force_tiny(oracle_mod):
     # the fp64 summation order of the matmul)
     d2, b2 = oracle_mod.gemm_reference(qa, qb, rows=np.array([4, 1]))
     assert (np.abs(d2 - d[[4, 1]]) <= 1e-14 * b2).all()
+
+
+# ---------------------------------------------------------------------------
+# W4A16 reference: BF16 rounding and the product with the BF16 weights
+# ---------------------------------------------------------------------------
+def test_bf16_round_matches_torch():
+    rng = np.random.default_rng(11)
+    x = np.concatenate([(rng.standard_normal(200000) * 10.0 ** rng.integers(-30, 30, 200000)).astype(np.float32),
+                        np.array([0.0, -0.0, 1.0, 1.00390625, 1.005859375, 3.4e38, 1e-40], dtype=np.float32)])
+    want = torch.from_numpy(x).to(torch.bfloat16).to(torch.float32).numpy()
+    got = oracle.bf16_round(x)
+    assert (got.view(np.uint32) == want.view(np.uint32)).all()
+
+
+def test_w4a16_reference_brute_force():
+    """Tiny case against a Python loop over exact rationals."""
+    from fractions import Fraction
+    rng = np.random.default_rng(12)
+    M, N, K = 2, 3, 32
+    x = torch.from_numpy(rng.standard_normal((M, K)).astype(np.float32)).to(torch.bfloat16).float().numpy()
+    qw = oracle.quantize(rng.standard_normal((N, K)).astype(np.float32))
+    w = oracle.bf16_round(oracle.dequantize(qw.codes, qw.scales, qw.g))
+    d, bound = oracle.w4a16_reference(x, qw)
+    for m in range(M):
+        for n in range(N):
+            exact = sum(Fraction(float(x[m, k])) * Fraction(float(w[n, k])) for k in range(K))
+            assert abs(float(exact) - d[m, n]) <= 1e-12 * max(1.0, bound[m, n])
+
+
+def test_w4a16_reference_constant_weights_closed_form():
+    """A constant weight tensor decodes to one value c everywhere, so each
+    output is c times the row sum of X."""
+    rng = np.random.default_rng(13)
+    qw = oracle.quantize(np.full((48, 64), 0.3, dtype=np.float32))
+    w = oracle.bf16_round(oracle.dequantize(qw.codes, qw.scales, qw.g))
+    c = float(w[0, 0])
+    assert (w == np.float32(c)).all() and abs(c - 0.3) < 0.3 / 64
+    x = torch.from_numpy(rng.standard_normal((5, 64)).astype(np.float32)).to(torch.bfloat16).float().numpy()
+    d, _ = oracle.w4a16_reference(x, qw)
+    want = c * x.astype(np.float64).sum(axis=1)
+    assert np.allclose(d, want[:, None], rtol=0, atol=1e-12)
