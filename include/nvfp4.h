@@ -179,6 +179,31 @@ nvfp4_status nvfp4_rht_quantize(const void* x, nvfp4_dtype xt, int64_t rows, int
 nvfp4_status nvfp4_dequantize(const nvfp4_tensor* q, void* y, nvfp4_dtype yt, void* stream);
 
 /*
+ * nvfp4_w4a16_gemm - weight-only NVFP4 GEMM (W4A16) for BF16 activations:
+ *   y[m][n] = sum_k x[m][k] * W_hat[n][k],  W_hat = BF16(fl(fl(value * s_b) * g)),
+ * the weights dequantized exactly as nvfp4_dequantize with BF16 output, the
+ * products and sums in FP32.  The serving variant for GPUs without FP4
+ * tensor cores (the hyper.ai story on the Nemotron 3 Ultra NVFP4 checkpoint:
+ * Blackwell computes W4A4, Hopper serving switches to W4A16; "BF16 vs NVFP4
+ * with Nemotron 3.5 Lightning", "Key takeaways").  On this GPU it serves
+ * decode-sized M, where it streams the 4.5-bit weights once.
+ *   x    device BF16, row-major [M][ldx], ldx >= W->cols, 16-byte aligned,
+ *        ldx % 8 == 0.  Only NVFP4_BF16 is accepted for xt.
+ *   W    host struct with device buffers: N = W->rows output features,
+ *        K = W->cols (% 16 == 0); codes, scales, global_scale read (1D or 2D
+ *        blocks: the scale layout holds a byte per row and block either way).
+ *   y    device, row-major [M][ldy] of dtype yt (F32 or BF16, rounded to
+ *        nearest even), ldy >= N, aligned to its element.  Every element of
+ *        the M x N result is written; the columns beyond N are not touched.
+ *   M = 0 or N = 0 launches nothing.  K = 0 writes zeros.
+ * Errors: NVFP4_ERR_INVALID_ARG (NULL buffer, bad dtype, ld too small),
+ * NVFP4_ERR_UNSUPPORTED_SHAPE (K % 16), NVFP4_ERR_MISALIGNED; nothing is
+ * launched on an argument error.
+ */
+nvfp4_status nvfp4_w4a16_gemm(const void* x, nvfp4_dtype xt, int64_t M, int64_t ldx, const nvfp4_tensor* W, void* y,
+                              nvfp4_dtype yt, int64_t ldy, void* stream);
+
+/*
  * nvfp4_transpose_2d - the NVFP4 tensor of x^T from that of x, for a tensor
  * quantized with 2D 16x16 blocks (the Dgrad operand W^T from the weight's
  * forward quantization; "NVIDIA Introduces a 4-Bit Pretraining Methodology

@@ -77,9 +77,11 @@ def lib() -> ctypes.CDLL:
         L.nvfp4_gemm_amax.argtypes = [ctypes.POINTER(CTensor), ctypes.POINTER(CTensor), P, ctypes.c_int, I64, P, P]
         L.nvfp4_gemm_grouped.argtypes = [ctypes.c_int, ctypes.POINTER(CTensor), ctypes.POINTER(CTensor),
                                          ctypes.POINTER(ctypes.c_void_p), ctypes.c_int, P]
+        L.nvfp4_w4a16_gemm.argtypes = [P, ctypes.c_int, I64, I64, ctypes.POINTER(CTensor), P, ctypes.c_int, I64, P]
         L.nvfp4_sync_check.argtypes = [P]
         for fn in ("nvfp4_amax", "nvfp4_quantize", "nvfp4_quantize_grouped", "nvfp4_rht_quantize", "nvfp4_dequantize",
-                   "nvfp4_transpose_2d", "nvfp4_gemm", "nvfp4_gemm_amax", "nvfp4_gemm_grouped", "nvfp4_sync_check"):
+                   "nvfp4_transpose_2d", "nvfp4_gemm", "nvfp4_gemm_amax", "nvfp4_gemm_grouped", "nvfp4_w4a16_gemm",
+                   "nvfp4_sync_check"):
             getattr(L, fn).restype = ctypes.c_int
         L.nvfp4_status_string.argtypes = [ctypes.c_int]
         L.nvfp4_status_string.restype = ctypes.c_char_p
@@ -282,6 +284,20 @@ def gemm_grouped(a: list, b: list, out_dtype=torch.bfloat16, out: list | None = 
     CB = (CTensor * max(n, 1))(*[x.c() for x in b])
     D = (ctypes.c_void_p * max(n, 1))(*[o.data_ptr() for o in out])
     _check(lib().nvfp4_gemm_grouped(n, CA, CB, D, _dtype_code(out_dtype), _stream(stream)), "nvfp4_gemm_grouped")
+    return out
+
+
+def w4a16_gemm(x: torch.Tensor, w: NVFP4Tensor, out_dtype=torch.bfloat16, out: torch.Tensor | None = None,
+               stream=None) -> torch.Tensor:
+    """nvfp4_w4a16_gemm: y [M, N] = x (BF16, M x K) * W_hat^T, W_hat the BF16
+    dequantization of the NVFP4 weight w (N x K), FP32 accumulation."""
+    if x.dtype != torch.bfloat16 or x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be a 2D BF16 tensor with unit column stride")
+    if out is None:
+        out = torch.empty((x.shape[0], w.rows), dtype=out_dtype, device=x.device)
+    cw = w.c()
+    _check(lib().nvfp4_w4a16_gemm(_ptr(x), BF16, x.shape[0], x.stride(0), ctypes.byref(cw), _ptr(out),
+                                  _dtype_code(out.dtype), out.stride(0), _stream(stream)), "nvfp4_w4a16_gemm")
     return out
 
 

@@ -272,6 +272,32 @@ nvfp4_status nvfp4_dequantize(const nvfp4_tensor* q, void* y, nvfp4_dtype yt, vo
   return e == cudaSuccess ? NVFP4_OK : cuda_fail(e, "dequantize launch");
 }
 
+nvfp4_status nvfp4_w4a16_gemm(const void* x, nvfp4_dtype xt, int64_t M, int64_t ldx, const nvfp4_tensor* W, void* y,
+                              nvfp4_dtype yt, int64_t ldy, void* stream) {
+  nvfp4_status st = check_tensor_buffers(W, "W");
+  if (st != NVFP4_OK) return st;
+  if (xt != NVFP4_BF16) return fail(NVFP4_ERR_INVALID_ARG, "x must be BF16");
+  if (yt != NVFP4_F32 && yt != NVFP4_BF16) return fail(NVFP4_ERR_INVALID_ARG, "output dtype must be F32 or BF16");
+  if (M < 0) return fail(NVFP4_ERR_INVALID_ARG, "negative M");
+  const int64_t N = W->rows, K = W->cols;
+  if (K % 16) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "K (W->cols) must be a multiple of 16");
+  if (ldx < K) return fail(NVFP4_ERR_INVALID_ARG, "ldx < K");
+  if (ldy < N) return fail(NVFP4_ERR_INVALID_ARG, "ldy < N");
+  if (M == 0 || N == 0) return NVFP4_OK;
+  if (!y) return fail(NVFP4_ERR_INVALID_ARG, "y is NULL");
+  if (reinterpret_cast<uintptr_t>(y) % (yt == NVFP4_BF16 ? 2 : 4))
+    return fail(NVFP4_ERR_MISALIGNED, "y must be aligned to its element");
+  if (K > 0) {
+    if (!x) return fail(NVFP4_ERR_INVALID_ARG, "x is NULL");
+    if (!aligned16(x) || ldx % 8) return fail(NVFP4_ERR_MISALIGNED, "x must be 16-byte aligned with ldx % 8 == 0");
+  }
+  if (K / 16 > ((int64_t)1 << 26) || cdiv(N, 16) > ((int64_t)1 << 31) - 1)
+    return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "tensor too large for one launch");
+  cudaError_t e = nvfp4::launch_w4a16(x, M, ldx, W->codes, W->scales, W->global_scale, N, K, y, yt == NVFP4_BF16, ldy,
+                                      reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? NVFP4_OK : cuda_fail(e, "w4a16 launch");
+}
+
 namespace {
 nvfp4_status run_gemm(const nvfp4_tensor* A, const nvfp4_tensor* B, void* D, nvfp4_dtype dt, int64_t ldd,
                       float* amax_out, void* stream) {

@@ -45,6 +45,8 @@ cudaError_t launch_quantize(const QuantArgs& a, bool bf16, bool transpose, bool 
 cudaError_t launch_empty_scalars(float* amax, float* g, cudaStream_t s);
 cudaError_t launch_dequantize(const uint8_t* codes, const uint8_t* scales, const float* g, int64_t R, int64_t K,
                               void* y, bool bf16_out, cudaStream_t s);
+cudaError_t launch_w4a16(const void* x, int64_t M, int64_t ldx, const uint8_t* codes, const uint8_t* scales,
+                         const float* g, int64_t N, int64_t K, void* y, bool out_bf16, int64_t ldy, cudaStream_t s);
 cudaError_t launch_transpose_2d(const uint8_t* codes, const uint8_t* scales, const float* g, const float* amax,
                                 int64_t R, int64_t K, uint8_t* codes_t, uint8_t* scales_t, float* g_t, float* amax_t,
                                 cudaStream_t s);

@@ -30,7 +30,7 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     for required in ["nvfp4_amax", "nvfp4_quantize", "nvfp4_quantize_grouped", "nvfp4_rht_quantize", "nvfp4_dequantize",
                      "nvfp4_transpose_2d", "nvfp4_gemm", "nvfp4_gemm_amax",
-                     "nvfp4_gemm_grouped", "nvfp4_codes_bytes", "nvfp4_scales_bytes", "nvfp4_sync_check",
+                     "nvfp4_gemm_grouped", "nvfp4_w4a16_gemm", "nvfp4_codes_bytes", "nvfp4_scales_bytes", "nvfp4_sync_check",
                      "nvfp4_status_string", "nvfp4_last_error"]:
         assert required in names
 
@@ -165,3 +165,24 @@ def test_gemm_amax_argument_errors(L):
     assert L.nvfp4_gemm_amax(ctypes.byref(A), ctypes.byref(B), D, nv.BF16, 256, None, None) == 1   # amax_out NULL
     assert L.nvfp4_gemm_amax(ctypes.byref(A), ctypes.byref(_fake_tensor(256, 512)), D, nv.BF16, 256,
                              ctypes.c_void_p(0x5000000), None) == 1                                  # K differs
+
+
+def test_w4a16_argument_errors(L):
+    W = _fake_tensor(256, 512)
+    x, y = ctypes.c_void_p(0x4000000), ctypes.c_void_p(0x5000000)
+    w = ctypes.byref(W)
+    call = L.nvfp4_w4a16_gemm
+    assert call(x, nv.F32, 4, 512, w, y, nv.BF16, 256, None) == 1                      # x must be BF16
+    assert call(x, nv.BF16, 4, 512, w, y, 9, 256, None) == 1                           # output dtype
+    assert call(x, nv.BF16, -1, 512, w, y, nv.BF16, 256, None) == 1                    # negative M
+    assert call(x, nv.BF16, 4, 500, w, y, nv.BF16, 256, None) == 1                     # ldx < K
+    assert call(x, nv.BF16, 4, 512, w, y, nv.BF16, 200, None) == 1                     # ldy < N
+    assert call(x, nv.BF16, 4, 512, None, y, nv.BF16, 256, None) == 1                  # W NULL
+    assert call(x, nv.BF16, 4, 40, ctypes.byref(_fake_tensor(256, 40)), y, nv.BF16, 256, None) == 2   # K % 16
+    assert call(ctypes.c_void_p(0x4000008), nv.BF16, 4, 512, w, y, nv.BF16, 256, None) == 3          # x alignment
+    assert call(x, nv.BF16, 4, 516, w, y, nv.BF16, 256, None) == 3                     # ldx % 8
+    assert call(x, nv.BF16, 4, 512, w, ctypes.c_void_p(0x5000001), nv.BF16, 256, None) == 3          # y alignment
+    assert call(x, nv.BF16, 4, 512, w, ctypes.c_void_p(0x5000002), nv.F32, 256, None) == 3
+    assert call(x, nv.BF16, 4, 512, w, None, nv.BF16, 256, None) == 1                  # y NULL
+    assert call(None, nv.BF16, 4, 512, w, y, nv.BF16, 256, None) == 1                  # x NULL
+    assert call(x, nv.BF16, 0, 512, w, None, nv.BF16, 256, None) == 0                  # M = 0: nothing to do
