@@ -47,6 +47,9 @@ WORKLOADS = {
     "moe": dict(E=64, M=512, N=1536, K=4096, desc="MoE experts: 64 x W_e 4096x1536 bf16 0.02*t(3) quantized as W_e^T "
                                                    "(1D along K=4096, Four-over-Six), 64 x X_e 512x4096 bf16 N(0,1) "
                                                    "(1D, max-6), grouped GEMM 64 x (512x1536x4096) BF16 out"),
+    "w4a16": dict(L=8, M=4, N=14336, K=4096, desc="W4A16 decode: 8 layers' Llama-3-8B MLP up-projection weights "
+                                                  "14336x4096 (bf16 N(0,0.02), quantized once with 2D blocks), "
+                                                  "X 4x4096 bf16 N(0,1) + 0.1% channels x20, BF16 out"),
 }
 
 
@@ -642,11 +645,147 @@ def run_moe(args, rank, world, local_rank):
     return line
 
 
+def run_w4a16(args, rank, world, local_rank):
+    """The weight-only decode configuration: per step, M tokens through L
+    layers' NVFP4 weights (one W4A16 launch per layer, each on its own copy
+    of the weight, so no launch finds its weight in L2).  Weights are
+    quantized once, outside the step, as a serving deployment does."""
+    import nvfp4_bit_block_02_b300 as nv
+    import synthetic
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    c = WORKLOADS["w4a16"]
+    L, M, N, K = c["L"], c["M"], c["N"], c["K"]
+    wl = synthetic.llama8b_fprop(m=M, n=N, k=K)
+    x_h = wl.tensors["X"].pin_memory()
+    x = x_h.to(dev)
+    w_bf16 = wl.tensors["W"].to(dev)
+    q0 = nv.quantize(w_bf16, block="2d")
+    qs = [nv.NVFP4Tensor(q0.codes.clone(), q0.scales.clone(), q0.global_scale.clone(), q0.amax.clone(), N, K)
+          for _ in range(L)]
+    ys = [torch.empty((M, N), dtype=torch.bfloat16, device=dev) for _ in range(L)]
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    nv.sync_check()
+
+    def step(xm, outs):
+        for l in range(L):
+            nv.w4a16_gemm(xm, qs[l], out=outs[l])
+
+    stream = torch.cuda.current_stream(dev)
+    side = torch.cuda.Stream(dev)
+
+    def graph_of(fn):
+        for _ in range(args.warmup):
+            fn()
+        side.wait_stream(stream)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side):
+                fn()
+        stream.wait_stream(side)
+        for _ in range(args.warmup):
+            g.replay()
+        return g
+
+    def timed(g, steps):
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+        for i in range(steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            g.replay()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        return [e[0].elapsed_time(e[1]) for e in ev]
+
+    g_step = graph_of(lambda: step(x, ys))
+    nv.sync_check(stream)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    t_step = timed(g_step, args.steps)
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop() if sampler else None
+    nv.sync_check(stream)
+    step_ms = sum(t_step)
+    # other decode batch sizes, and a BF16 GEMM of the same shape (cuBLAS, for context)
+    comps = {}
+    for m in (1, 4, 16):
+        xm = synthetic.llama8b_fprop(m=m, n=16, k=K).tensors["X"].to(dev)
+        outs = [torch.empty((m, N), dtype=torch.bfloat16, device=dev) for _ in range(L)]
+        ms = statistics.mean(timed(graph_of(lambda: step(xm, outs)), max(10, args.steps // 4))) / L
+        b = N * K // 2 + nv.scales_bytes(N, K) + m * K * 2 + m * N * 2
+        comps[f"w4a16_M{m}"] = {"us_per_launch": round(ms * 1e3, 2), "GB_s": round(b / (ms * 1e-3) / 1e9, 1),
+                                "TFLOP_s": round(2.0 * m * N * K / (ms * 1e-3) / 1e12, 2)}
+    w_layers = [w_bf16.clone() for _ in range(L)]
+    yb = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    ms_bf16 = statistics.mean(timed(graph_of(lambda: [torch.matmul(x, wl_.t(), out=yb) for wl_ in w_layers]),
+                                    max(10, args.steps // 4))) / L
+    comps["bf16_cublas_same_shape"] = {"us_per_launch": round(ms_bf16 * 1e3, 2),
+                                       "GB_s": round((N * K * 2 + M * K * 2 + M * N * 2) / (ms_bf16 * 1e-3) / 1e9, 1),
+                                       "note": "torch.matmul on the BF16 weight (context, not the path)"}
+    del w_layers
+    # end to end: H2D of the step's activations, D2H of every layer's output
+    y_h = torch.empty((L, M, N), dtype=torch.bfloat16, pin_memory=True)
+    e2e_steps = 20
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        x.copy_(x_h, non_blocking=True)
+        step(x, ys)
+        for l in range(L):
+            y_h[l].copy_(ys[l], non_blocking=True)
+    torch.cuda.synchronize(dev)
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    step_ms, e2e_s = max_over_ranks([step_ms, e2e_s], world)
+    if rank != 0:
+        return None
+    pk, pk_src = peaks()
+    flops = 2.0 * L * M * N * K
+    ms_per_step = step_ms / args.steps
+    abytes = N * K // 2 + nv.scales_bytes(N, K) + M * K * 2 + M * N * 2
+    gbs = abytes / (ms_per_step / L * 1e-3) / 1e9
+    line = {
+        "metric": "W4A16 decode TFLOP/s (weight-stream GB/s as % of B300 HBM roofline)",
+        "value": round(world * flops / (ms_per_step * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 activations x fp4(e2m1)+e4m3 weights decoded to bf16, fp32 accumulate; bf16 out",
+        "data": "synthetic (seeded numpy draws, the pages' shapes; no model weights)",
+        "config": {"workload": "w4a16", "layers": L, "tokens": M, "N": N, "K": K, "desc": c["desc"],
+                   "l2": f"256 MiB flush write between steps (outside the timed events); {L} weight copies "
+                         f"of {abytes / 1e6:.1f} MB each",
+                   "timing": "the step (one launch per layer) captured once as a CUDA graph, replayed between "
+                             "CUDA events",
+                   "value_is": "2*L*M*N*K / step time"},
+        "components": comps,
+        "roofline": {"bound": "hbm", "kernel": "k_w4a16 (one layer)", "achieved": round(gbs, 1),
+                     "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4),
+                     "traffic": ncu_traffic("k_w4a16", source_hash("w4a16.cu", "nvfp4_device.cuh")),
+                     "algorithmic_bytes_per_launch": abytes, "peak_source": f"{pk_src} copy bandwidth"},
+        "e2e": {"value": round(world * flops / e2e_s / 1e12, 3), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": int(x_h.numel() * 2), "d2h_bytes_per_step": int(y_h.numel() * 2)},
+        "gpu_launches": L * args.steps * world,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline("w4a16")
+    return line
+
+
 # --------------------------------------------------------------------------
 # the oracle on the host cores (the reference arm and the cpu_baseline key)
 # --------------------------------------------------------------------------
 def _oracle_inputs(workload: str):
     import synthetic
+    if workload == "w4a16":
+        c = WORKLOADS["w4a16"]
+        wl = synthetic.llama8b_fprop(m=c["M"], n=c["N"], k=c["K"])
+        return wl.tensors["X"].to(torch.float32).numpy(), wl.tensors["W"].to(torch.float32).numpy()
     if workload == "moe":
         c = WORKLOADS["moe"]
         wl = synthetic.moe(1, c["M"], c["K"], c["N"])
@@ -670,6 +809,12 @@ def _oracle_sample(workload: str, X, W, rx: int, rw: int, rg: int):
     import oracle
     c = WORKLOADS[workload]
     M, N = c["M"], c["N"]
+    if workload == "w4a16":   # rw weight rows (quantized outside the timing); scaled to N rows and L layers
+        qw = oracle.quantize(W[:rw], block2d=True)
+        t0 = time.perf_counter()
+        oracle.w4a16_reference(X, qw)
+        t1 = time.perf_counter()
+        return c["L"] * (t1 - t0) * N / rw, t1 - t0
     if workload == "moe":   # one expert: W^T with Four-over-Six, X max-6; scaled to E experts
         E, Mt = c["E"], c["M"]
         t0 = time.perf_counter()
@@ -700,14 +845,23 @@ def _oracle_sample(workload: str, X, W, rx: int, rw: int, rg: int):
 
 def _flops(workload: str) -> float:
     c = WORKLOADS[workload]
-    return 2.0 * c.get("E", 1) * c["M"] * c["N"] * c["K"]
+    return 2.0 * c.get("E", 1) * c.get("L", 1) * c["M"] * c["N"] * c["K"]
 
 
 # per workload: the slice the oracle is timed on (see _oracle_sample), as (rx, rw, rg)
 _CPU_SAMPLE = {"pr1": (256, 256, 256), "llama8b": (8192, 14336, 2048), "llama405b": (2048, 4096, 256),
-               "wgrad": (2048, 1024, 512), "moe": (0, 0, 256)}
+               "wgrad": (2048, 1024, 512), "moe": (0, 0, 256), "w4a16": (0, 14336, 0)}
 _REF_SAMPLE = {"pr1": (256, 256, 64), "llama8b": (512, 896, 64), "llama405b": (128, 256, 16),
-               "wgrad": (256, 64, 64), "moe": (0, 0, 16)}
+               "wgrad": (256, 64, 64), "moe": (0, 0, 16), "w4a16": (0, 2048, 0)}
+
+
+def _sample_desc(workload: str, rx: int, rw: int, rg: int) -> str:
+    if workload == "w4a16":
+        return (f"w4a16: oracle W4A16 product (BF16-rounded decode, fp64 matmul) of the {WORKLOADS['w4a16']['M']} "
+                f"tokens with {rw} weight rows (quantized outside the timing), scaled to all rows and "
+                f"{WORKLOADS['w4a16']['L']} layers")
+    return (f"{workload}: oracle quantize of a slice (rx={rx}, rw={rw}) and fp64 GEMM of {rg} output rows, "
+            "each part scaled to the whole step (MoE: one expert, scaled to 64)")
 
 
 def cpu_baseline(workload: str):
@@ -720,8 +874,7 @@ def cpu_baseline(workload: str):
     t_step, spent = _oracle_sample(workload, X, W, rx, rw, rg)
     return {"value": round(_flops(workload) / t_step / 1e12, 6), "unit": "TFLOP/s",
             "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
-            "sample": f"{workload}: oracle quantize of a slice (rx={rx}, rw={rw}) and fp64 GEMM of {rg} output rows, "
-                      "each part scaled to the whole step (MoE: one expert, scaled to 64)",
+            "sample": _sample_desc(workload, rx, rw, rg),
             "sample_seconds": round(spent, 2), "extrapolated_step_seconds": round(t_step, 2)}
 
 
@@ -733,8 +886,7 @@ def run_reference(args):
     oracle.build()
     X, W = _oracle_inputs(args.workload)
     rx, rw, rg = _REF_SAMPLE[args.workload]
-    sample = (f"per step: {args.workload} oracle quantize of a slice (rx={rx}, rw={rw}) and fp64 GEMM of {rg} "
-              "output rows, each part scaled to the whole step (MoE: one expert, scaled to 64)")
+    sample = "per step: " + _sample_desc(args.workload, rx, rw, rg)
     for _ in range(args.warmup):
         _oracle_sample(args.workload, X, W, rx, rw, rg)
     t_steps = [_oracle_sample(args.workload, X, W, rx, rw, rg)[0] for _ in range(max(1, args.steps))]
@@ -771,7 +923,8 @@ def main():
         return
     if world > 1:
         torch.distributed.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
-    line = (run_moe if args.workload == "moe" else run_ours)(args, rank, world, local_rank)
+    run = {"moe": run_moe, "w4a16": run_w4a16}.get(args.workload, run_ours)
+    line = run(args, rank, world, local_rank)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
