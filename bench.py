@@ -70,16 +70,16 @@ def source_hash(*names):
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel: str, src_hash: str):
+def ncu_traffic(kernel: str, src_hash: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source."""
+    on the current kernel source and on this workload's launch."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
     e = d.get(kernel)
-    if not e or e.get("source_hash") != src_hash:
+    if not e or e.get("source_hash") != src_hash or e.get("bench_workload") != workload:
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -421,8 +421,8 @@ def run_ours(args, rank, world, local_rank):
     fp4_burst = pk["bf16_tflops"] * FP4_OVER_BF16
     fp4_peak = (pk["bf16_tflops_sustained"] if sustained else pk["bf16_tflops"]) * FP4_OVER_BF16
     gemm_tflops = flops / (gemm_ms * 1e-3) / 1e12
-    traffic = ncu_traffic("k_gemm", source_hash("gemm.cu", "gemm.h"))
-    q_traffic = ncu_traffic("k_quant_rows", source_hash("quantize.cu", "nvfp4_device.cuh"))
+    traffic = ncu_traffic("k_gemm", source_hash("gemm.cu", "gemm.h"), args.workload)
+    q_traffic = ncu_traffic("k_quant_rows", source_hash("quantize.cu", "nvfp4_device.cuh"), args.workload)
     hbm = pk["hbm_gbs"]
     enc_line = {}
     if enc:
@@ -765,7 +765,7 @@ def run_w4a16(args, rank, world, local_rank):
         "components": comps,
         "roofline": {"bound": "hbm", "kernel": "k_w4a16 (one layer)", "achieved": round(gbs, 1),
                      "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4),
-                     "traffic": ncu_traffic("k_w4a16", source_hash("w4a16.cu", "nvfp4_device.cuh")),
+                     "traffic": ncu_traffic("k_w4a16", source_hash("w4a16.cu", "nvfp4_device.cuh"), "w4a16"),
                      "algorithmic_bytes_per_launch": abytes, "peak_source": f"{pk_src} copy bandwidth"},
         "e2e": {"value": round(world * flops / e2e_s / 1e12, 3), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": int(x_h.numel() * 2), "d2h_bytes_per_step": int(y_h.numel() * 2)},
