@@ -85,8 +85,8 @@ template <typename T>
 __global__ void __launch_bounds__(256) k_amax_grouped(const __grid_constant__ GroupQuant g) {
   constexpr int VEC = 16 / sizeof(T);
   const uint32_t total = g.amax_start[g.count];
+  uint32_t e = 0;  // t only grows, so the group search resumes where it stopped
   for (uint32_t t = blockIdx.x; t < total; t += gridDim.x) {
-    uint32_t e = 0;
     while (t >= g.amax_start[e + 1]) ++e;
     const QuantArgs& a = g.a[e];
     const int64_t nvec = a.C_in / VEC, ldv = a.ld / VEC;
@@ -211,9 +211,11 @@ struct Groups {
   const GroupQuant& g;
   __device__ explicit Groups(const GroupQuant& gq) : g(gq) {}
   __device__ const QuantArgs& args(const Ref& r) const { return g.a[r.e]; }
-  __device__ bool locate(uint32_t t, Ref& r) const {
+  // e0: a group at or before tile t's (a CTA's tiles only move forward, so
+  // the search resumes from the previous tile's group)
+  __device__ bool locate(uint32_t t, Ref& r, uint32_t e0 = 0) const {
     if (t >= g.tile_start[g.count]) return false;
-    uint32_t e = 0;
+    uint32_t e = e0;
     while (t >= g.tile_start[e + 1]) ++e;
     const uint32_t local = t - g.tile_start[e];
     r.t = t;
@@ -223,7 +225,7 @@ struct Groups {
     return true;
   }
   __device__ bool first(Ref& r) const { return locate(blockIdx.x, r); }
-  __device__ bool next(const Ref& c, Ref& n) const { return locate(c.t + gridDim.x, n); }
+  __device__ bool next(const Ref& c, Ref& n) const { return locate(c.t + gridDim.x, n, c.e); }
   // the first tile of a group publishes its g and amax
   __device__ bool owns_scalars(const Ref& r) const { return r.t == g.tile_start[r.e]; }
 };
@@ -258,6 +260,7 @@ __device__ __forceinline__ void quant_rows_body(const Src& src, const QuantArgs&
   };
   if constexpr (!AMAX_ONLY && !Src::kGrouped) set_scale(a0, blockIdx.x == 0);
   float run_max = 0.0f;
+  [[maybe_unused]] uint32_t scale_group = 0xFFFFFFFFu;  // the group whose scale g, g6, g4 hold
 
   auto load = [&](const typename Src::Ref& ref, RawBlock<T> (&raw)[2]) {
     const QuantArgs& a = src.args(ref);
@@ -282,7 +285,11 @@ __device__ __forceinline__ void quant_rows_body(const Src& src, const QuantArgs&
     if (have_next) load(nref, nxt);
     const QuantArgs& a = src.args(ref);
     const uint32_t R = (uint32_t)a.R, KB = (uint32_t)(a.K / 16), nka = (KB + 3) / 4;
-    if constexpr (!AMAX_ONLY && Src::kGrouped) set_scale(a, src.owns_scalars(ref));
+    if constexpr (!AMAX_ONLY && Src::kGrouped) {
+      const bool owns = src.owns_scalars(ref);
+      if (owns || ref.e != scale_group) set_scale(a, owns);
+      scale_group = ref.e;
+    }
     float v[2][16];
     bool valid[2];
     uint32_t r[2];
@@ -444,6 +451,7 @@ __device__ __forceinline__ void quant_cols_body(const Src& src, const QuantArgs&
   };
   if constexpr (!AMAX_ONLY && !Src::kGrouped) set_scale(a0, blockIdx.x == 0);
   float run_max = 0.0f;
+  [[maybe_unused]] uint32_t scale_group = 0xFFFFFFFFu;  // the group whose scale g, g6, g4 hold
 
   auto load = [&](const typename Src::Ref& ref, uint4 (&raw)[NV]) {
     const QuantArgs& a = src.args(ref);
@@ -480,7 +488,11 @@ __device__ __forceinline__ void quant_cols_body(const Src& src, const QuantArgs&
     const uint32_t Tt = (uint32_t)a.R_in, N = (uint32_t)a.C_in;
     const int64_t K = Tt;
     const uint32_t KB = Tt / 16, nka = (KB + 3) / 4;
-    if constexpr (!AMAX_ONLY && Src::kGrouped) set_scale(a, src.owns_scalars(ref));
+    if constexpr (!AMAX_ONLY && Src::kGrouped) {
+      const bool owns = src.owns_scalars(ref);
+      if (owns || ref.e != scale_group) set_scale(a, owns);
+      scale_group = ref.e;
+    }
     const uint32_t n0 = ref.tx * 128;
     const uint32_t kb = ref.ty * 4 + kbl;
     float v[2][16];
