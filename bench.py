@@ -385,16 +385,34 @@ def run_ours(args, rank, world, local_rank):
     t_parts = [[evc[i][j].elapsed_time(evc[i][j + 1]) for i in range(args.steps)] for j in range(3)]
     t_gm = t_parts[2]
     enc = encode_rates(nv, x, w, dev) if rank == 0 and args.workload in ("llama8b", "llama405b") else None
-    # end to end through the public API from pinned host buffers, D read back
+    # end to end through the public API from pinned host buffers, D read back.
+    # Every step uploads its X and W and reads back all of D.  The read-back
+    # runs on a stream of its own (the opposite direction of the host link),
+    # so the next step's upload and quantizations proceed meanwhile; only the
+    # GEMM that overwrites D waits for the previous read-back to finish.
     d_h = torch.empty((M, N), dtype=d.dtype, pin_memory=True)
+    d2h_stream = torch.cuda.Stream(dev)
     e2e_steps = max(2, min(args.steps, 5))
     torch.cuda.synchronize(dev)
     t0 = time.perf_counter()
+    d_free = None
     for _ in range(e2e_steps):
+        main = torch.cuda.current_stream(dev)
         x.copy_(x_h, non_blocking=True)
         w.copy_(w_h, non_blocking=True)
-        step()
-        d_h.copy_(d, non_blocking=True)
+        fork_stream.wait_stream(main)
+        plan["parts"][0][1]()
+        with torch.cuda.stream(fork_stream):
+            plan["parts"][1][1]()
+        main.wait_stream(fork_stream)
+        if d_free is not None:
+            main.wait_event(d_free)
+        plan["parts"][2][1]()
+        d2h_stream.wait_stream(main)
+        with torch.cuda.stream(d2h_stream):
+            d_h.copy_(d, non_blocking=True)
+            d_free = torch.cuda.Event()
+            d_free.record(d2h_stream)
     torch.cuda.synchronize(dev)
     e2e_s = (time.perf_counter() - t0) / e2e_steps
 
@@ -583,17 +601,33 @@ def run_moe(args, rank, world, local_rank):
         se46 += float(((nv.dequantize(qw[e]) - ref) ** 2).double().sum())
         se6 += float(((nv.dequantize(q6[e]) - ref) ** 2).double().sum())
     nv.sync_check()
-    # end to end: H2D of every expert's W and X from pinned memory, D2H of every D
+    # end to end: H2D of every expert's W and X from pinned memory, D2H of
+    # every D; the read-back runs on its own stream (the other direction of the
+    # host link) and only the next grouped GEMM, which overwrites D, waits for it
     d_h = torch.empty((E, M, N), dtype=torch.bfloat16, pin_memory=True)
+    d2h_stream = torch.cuda.Stream(dev)
     e2e_steps = 2
     torch.cuda.synchronize(dev)
     t0 = time.perf_counter()
+    d_free = None
     for _ in range(e2e_steps):
+        main = torch.cuda.current_stream(dev)
         w.copy_(w_h, non_blocking=True)
         x.copy_(x_h, non_blocking=True)
-        step()
-        for e in range(E):
-            d_h[e].copy_(d[e], non_blocking=True)
+        fork_stream.wait_stream(main)
+        quant_w()
+        with torch.cuda.stream(fork_stream):
+            quant_x()
+        main.wait_stream(fork_stream)
+        if d_free is not None:
+            main.wait_event(d_free)
+        grouped()
+        d2h_stream.wait_stream(main)
+        with torch.cuda.stream(d2h_stream):
+            for e in range(E):
+                d_h[e].copy_(d[e], non_blocking=True)
+            d_free = torch.cuda.Event()
+            d_free.record(d2h_stream)
     torch.cuda.synchronize(dev)
     e2e_s = (time.perf_counter() - t0) / e2e_steps
     step_ms, e2e_s = max_over_ranks([step_ms, e2e_s], world)
