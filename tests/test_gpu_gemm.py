@@ -222,3 +222,47 @@ def test_gemm_grouped_moe_full_size_sampled():
         assert_same_quantized(qw[e], rw, f"W_{e}")
         rows = rng.choice(512, 32, replace=False)
         _sampled_check(rx, rw, outs[e], True, rows, f"expert {e}")
+
+
+def _rows_logical_scales(phys: np.ndarray, K: int, rows: np.ndarray) -> np.ndarray:
+    """The logical scale bytes [len(rows)][K/16] of the given rows, read out of
+    a physical buffer in the 128-row x 4-block atom layout of include/nvfp4.h."""
+    KB = K // 16
+    nka = (KB + 3) // 4
+    r = rows.astype(np.int64)[:, None]
+    kb = np.arange(KB, dtype=np.int64)[None, :]
+    off = ((r >> 7) * nka + (kb >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (kb & 3)
+    return phys[off]
+
+
+def test_llama405b_full_size_sampled():
+    """Llama-3.1-405B MLP fprop at full size: X 8192 x 16384 (1D), W 53248 x 16384
+    (2D), GEMM with BF16 out, all on the GPU.  Sampled X rows and sampled
+    16-row W groups are checked bit-exact against the oracle's quantization of
+    those rows with the whole tensor's amax; the GEMM outputs at those rows and
+    columns against the oracle's product of the same operands."""
+    wl = synthetic.llama405b_fprop()
+    X, W = wl.tensors["X"], wl.tensors["W"]
+    K = X.shape[1]
+    qx = nv.quantize(X.cuda())
+    qw = nv.quantize(W.cuda(), block="2d")
+    d = nv.gemm(qx, qw, out_dtype=torch.bfloat16)
+    nv.sync_check()
+    rng = np.random.default_rng(405)
+    rx = np.unique(np.concatenate([np.arange(64), np.arange(8192 - 64, 8192), rng.choice(8192, 128, replace=False)]))
+    groups = np.unique(np.concatenate([[0, 53248 // 16 - 1], rng.choice(53248 // 16, 14, replace=False)]))
+    rw = (groups[:, None] * 16 + np.arange(16)[None, :]).reshape(-1)
+    refs = {}
+    for name, full, q, rows, b2d in (("X", X, qx, rx, False), ("W", W, qw, rw, True)):
+        amax = float(torch.max(torch.abs(full)).float())
+        ref = oracle.quantize(full[rows].float().numpy(), block2d=b2d, amax=amax)
+        assert float(q.amax.cpu()[0]) == amax, f"405B {name}: amax"
+        assert float(q.global_scale.cpu()[0]) == ref.g, f"405B {name}: g"
+        codes = q.codes.cpu().numpy()[rows]
+        assert (codes == ref.codes).all(), f"405B {name}: {int((codes != ref.codes).sum())} code bytes differ"
+        sc = _rows_logical_scales(q.scales.cpu().numpy(), K, rows)
+        assert (sc == ref.scales).all(), f"405B {name}: {int((sc != ref.scales).sum())} scale bytes differ"
+        refs[name] = ref
+    ref, bound = oracle.gemm_reference(refs["X"], refs["W"])
+    got = d[torch.from_numpy(rx).cuda()][:, torch.from_numpy(rw).cuda()].float().cpu().numpy()
+    gemm_check(got, ref, bound, True, "405B fprop")
