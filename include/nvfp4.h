@@ -197,8 +197,8 @@ nvfp4_status nvfp4_dequantize(const nvfp4_tensor* q, void* y, nvfp4_dtype yt, vo
  *        the M x N result is written; the columns beyond N are not touched.
  *   M = 0 or N = 0 launches nothing.  K = 0 writes zeros.
  * Errors: NVFP4_ERR_INVALID_ARG (NULL buffer, bad dtype, ld too small),
- * NVFP4_ERR_UNSUPPORTED_SHAPE (K % 16), NVFP4_ERR_MISALIGNED; nothing is
- * launched on an argument error.
+ * NVFP4_ERR_UNSUPPORTED_SHAPE (K % 16, K > 2^28, ceil(N/16) >= 2^31),
+ * NVFP4_ERR_MISALIGNED; nothing is launched on an argument error.
  */
 nvfp4_status nvfp4_w4a16_gemm(const void* x, nvfp4_dtype xt, int64_t M, int64_t ldx, const nvfp4_tensor* W, void* y,
                               nvfp4_dtype yt, int64_t ldy, void* stream);

@@ -291,8 +291,9 @@ nvfp4_status nvfp4_w4a16_gemm(const void* x, nvfp4_dtype xt, int64_t M, int64_t 
     if (!x) return fail(NVFP4_ERR_INVALID_ARG, "x is NULL");
     if (!aligned16(x) || ldx % 8) return fail(NVFP4_ERR_MISALIGNED, "x must be 16-byte aligned with ldx % 8 == 0");
   }
-  if (K / 16 > ((int64_t)1 << 26) || cdiv(N, 16) > ((int64_t)1 << 31) - 1)
-    return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "tensor too large for one launch");
+  // the kernel's in-row offsets are 32-bit: scale bytes at (K/64) * 512 stay below 2^32 for K <= 2^28
+  if (K > ((int64_t)1 << 28) || cdiv(N, 16) > ((int64_t)1 << 31) - 1)
+    return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "tensor too large for one launch (K <= 2^28, N/16 < 2^31)");
   cudaError_t e = nvfp4::launch_w4a16(x, M, ldx, W->codes, W->scales, W->global_scale, N, K, y, yt == NVFP4_BF16, ldy,
                                       reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? NVFP4_OK : cuda_fail(e, "w4a16 launch");

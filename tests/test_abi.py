@@ -186,3 +186,6 @@ def test_w4a16_argument_errors(L):
     assert call(x, nv.BF16, 4, 512, w, None, nv.BF16, 256, None) == 1                  # y NULL
     assert call(None, nv.BF16, 4, 512, w, y, nv.BF16, 256, None) == 1                  # x NULL
     assert call(x, nv.BF16, 0, 512, w, None, nv.BF16, 256, None) == 0                  # M = 0: nothing to do
+    big = (1 << 28) + 16                                                                  # K beyond the kernel's offsets
+    assert call(x, nv.BF16, 1, big, ctypes.byref(_fake_tensor(16, big)), y, nv.BF16, 16, None) == 2
+    assert "too large" in L.nvfp4_last_error().decode()
