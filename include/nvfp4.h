@@ -1,5 +1,6 @@
 /*
- * nvfp4.h - C ABI of the B300 (sm_103a) NVFP4 quantizer and block-scaled GEMM.
+ * nvfp4.h - C ABI of the B300 (sm_103a) NVFP4 quantizer, block-scaled GEMM
+ * and weight-only (W4A16) GEMM.
  *
  * The format ("NVIDIA Introduces a 4-Bit Pretraining Methodology Using NVFP4",
  * section "Summary"): 16-element blocks of 4-bit E2M1 codes, one E4M3 scale per
