@@ -231,9 +231,14 @@ nvfp4_status nvfp4_transpose_2d(const nvfp4_tensor* q, nvfp4_tensor* qt, void* s
  * Nemotron 3 Ultra story says Blackwell runs natively.
  *   A  M x K NVFP4 (A->rows = M, A->cols = K), B  N x K NVFP4: both K-major.
  *   D  device row-major [M][ldd] of dtype dt (FP32 or BF16 rounded to nearest
- *      even from the fp32 result); ldd >= N, ldd * sizeof(dt) % 16 == 0.
- * Shape rules: K % 256 == 0, M % 128 == 0, N % 128 == 0 (every workload of the
- * recipe meets them); codes and scales 16-byte aligned.
+ *      even from the fp32 result); ldd >= N, ldd * sizeof(dt) % 16 == 0, D
+ *      16-byte aligned.  Exactly the M x N outputs are written.
+ * Shape rules: any M and N (up to 2^30), K % 64 == 0 (one tensor-core K-step);
+ * codes and scales 16-byte aligned.  The operands' scale padding (rows up to
+ * the next 128, blocks up to the next 4) must hold finite scales, as the
+ * quantizer writes them (0).  M = 0 or N = 0 writes nothing; K = 0 writes
+ * zeros.  The tile grid is 256 x 256 outputs per SM pair: shapes off that grid
+ * compute the padded tile and store only the valid part.
  */
 nvfp4_status nvfp4_gemm(const nvfp4_tensor* A, const nvfp4_tensor* B, void* D, nvfp4_dtype dt, int64_t ldd,
                         void* stream);
@@ -254,14 +259,20 @@ nvfp4_status nvfp4_gemm_amax(const nvfp4_tensor* A, const nvfp4_tensor* B, void*
 /*
  * nvfp4_gemm_grouped - `count` independent GEMMs D[e] = A[e] * B[e]^T in one
  * launch (routed experts).  A, B: host arrays of `count` tensors; D: host
- * array of `count` device pointers, each row-major [M_e][N_e] (ldd = N_e).
- * Every group follows the nvfp4_gemm shape rules; count <= NVFP4_MAX_GROUPS.
+ * array of `count` device pointers, each row-major [M_e][N_e] (ldd = N_e, so
+ * N_e * sizeof(dt) % 16 == 0).  Every group follows the nvfp4_gemm shape rules
+ * (M_e may be any count of routed tokens, including 0: the group is skipped)
+ * except that K_e must be positive; count <= NVFP4_MAX_GROUPS.
  */
 nvfp4_status nvfp4_gemm_grouped(int count, const nvfp4_tensor* A, const nvfp4_tensor* B, void* const* D,
                                 nvfp4_dtype dt, void* stream);
 
-/* Synchronise `stream`, then report (and clear) a pending CUDA error or a
- * GEMM pipeline timeout recorded on the device. */
+/* Synchronise `stream`, then report a pending CUDA error, or a GEMM pipeline
+ * timeout recorded on the current device.  The timeout word is one per
+ * device, shared by every GEMM launched on it from any stream or thread: it
+ * is read and cleared in one atomic exchange ordered on `stream`, so a timeout
+ * is reported once, by the first nvfp4_sync_check that follows it, and with
+ * GEMMs in flight on other streams it may belong to one of those. */
 nvfp4_status nvfp4_sync_check(void* stream);
 
 /* Human-readable status name (static string). */

@@ -128,8 +128,7 @@ nvfp4_status check_gemm_operands(const nvfp4_tensor* A, const nvfp4_tensor* B) {
   st = check_tensor_buffers(B, "B");
   if (st != NVFP4_OK) return st;
   if (A->cols != B->cols) return fail(NVFP4_ERR_INVALID_ARG, "A and B must have the same K (cols)");
-  if (A->cols < 256 || A->cols % 256) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "K must be a positive multiple of 256");
-  if (A->rows % 128 || B->rows % 128) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "M and N must be multiples of 128");
+  if (A->cols % 64) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "K must be a multiple of 64");
   if (A->rows > ((int64_t)1 << 30) || B->rows > ((int64_t)1 << 30) || A->cols > ((int64_t)1 << 30))
     return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "GEMM dimension too large");
   return NVFP4_OK;
@@ -310,6 +309,11 @@ nvfp4_status run_gemm(const nvfp4_tensor* A, const nvfp4_tensor* B, void* D, nvf
   if (ldd < B->rows) return fail(NVFP4_ERR_INVALID_ARG, "ldd < N");
   const int64_t es = dt == NVFP4_BF16 ? 2 : 4;
   if (!aligned16(D) || (ldd * es) % 16) return fail(NVFP4_ERR_MISALIGNED, "D must be 16-byte aligned, ldd*elsize % 16 == 0");
+  if (A->cols == 0) {  // an empty sum over k: D = 0 (and its amax 0, already zeroed by the caller)
+    cudaError_t e = cudaMemset2DAsync(D, (size_t)(ldd * es), 0, (size_t)(B->rows * es), (size_t)A->rows,
+                                      reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? NVFP4_OK : cuda_fail(e, "cudaMemset2DAsync(D)");
+  }
   const char* why = "";
   cudaError_t e = nvfp4::launch_gemm(operand(A), operand(B), D, ldd, dt == NVFP4_BF16,
                                      reinterpret_cast<cudaStream_t>(stream), &why, amax_out);
@@ -346,8 +350,11 @@ nvfp4_status nvfp4_gemm_grouped(int count, const nvfp4_tensor* A, const nvfp4_te
   for (int e = 0; e < count; ++e) {
     nvfp4_status st = check_gemm_operands(&A[e], &B[e]);
     if (st != NVFP4_OK) return fail(st, "group " + std::to_string(e) + ": " + g_last_error);
-    if (A[e].rows && B[e].rows && (!D[e] || !aligned16(D[e]) || (B[e].rows * es) % 16))
-      return fail(NVFP4_ERR_MISALIGNED, "group " + std::to_string(e) + ": D must be non-NULL and 16-byte aligned");
+    if (A[e].rows && B[e].rows && !D[e]) return fail(NVFP4_ERR_INVALID_ARG, "group " + std::to_string(e) + ": D is NULL");
+    if (A[e].rows && B[e].rows && (!aligned16(D[e]) || (B[e].rows * es) % 16))
+      return fail(NVFP4_ERR_MISALIGNED, "group " + std::to_string(e) + ": D must be 16-byte aligned with N*elsize % 16 == 0");
+    if (A[e].cols == 0 && A[e].rows && B[e].rows)
+      return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "group " + std::to_string(e) + ": K must be positive");
     ga[e] = operand(&A[e]);
     gb[e] = operand(&B[e]);
   }
@@ -362,16 +369,10 @@ nvfp4_status nvfp4_sync_check(void* stream) {
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "pending CUDA error");
-  unsigned int* w = nvfp4::device_error_word();
-  if (!w) return fail(NVFP4_ERR_CUDA, "device error word unavailable");
   unsigned int v = 0;
-  e = cudaMemcpy(&v, w, sizeof v, cudaMemcpyDeviceToHost);
+  e = nvfp4::take_device_error(reinterpret_cast<cudaStream_t>(stream), &v);
   if (e != cudaSuccess) return cuda_fail(e, "read device error word");
-  if (v) {
-    unsigned int zero = 0;
-    cudaMemcpy(w, &zero, sizeof zero, cudaMemcpyHostToDevice);
-    return fail(NVFP4_ERR_TIMEOUT, "a GEMM pipeline wait exceeded its limit");
-  }
+  if (v) return fail(NVFP4_ERR_TIMEOUT, "a GEMM pipeline wait exceeded its limit");
   return NVFP4_OK;
 }
 

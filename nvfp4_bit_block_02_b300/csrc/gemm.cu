@@ -40,13 +40,10 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 
 #include "gemm.h"
-
-#ifndef NVFP4_SFB_MODE
-#define NVFP4_SFB_MODE 0  // 0: every CTA holds the scales of all 256 B rows
-#endif
 
 namespace nvfp4 {
 namespace {
@@ -59,11 +56,7 @@ constexpr int STAGES = 5;
 constexpr int A_BYTES = BM * BKB;   // 16 KB
 constexpr int B_BYTES = BNH * BKB;  // 16 KB
 constexpr int SFA_BYTES = 4 * 512;  // 4 K-atoms of the CTA's 128 A rows
-#if NVFP4_SFB_MODE == 0
-constexpr int SFB_BYTES = 2 * 4 * 512;  // both 128-row blocks of B
-#else
-constexpr int SFB_BYTES = 4 * 512;
-#endif
+constexpr int SFB_BYTES = 2 * 4 * 512;  // both 128-row blocks of B: each CTA's MMA half reads all 256 columns' scales
 constexpr int EPI_WARPS = 8;
 constexpr int EPI_BYTES = 32 * 128;  // one 32-row x 128-byte box per epilogue warp
 constexpr int OFF_A = 0;
@@ -385,7 +378,7 @@ __device__ __forceinline__ void gemm_pairs(const Sched& sched, bool out_bf16, un
       const uint32_t lead_full0 = peer_addr(full0, 0);
       for (int t = first; t < num_tiles && !*abort_flag; t += step) {
         const Tile x = sched.get(t);
-        const int nk = x.K / 256;
+        const int nk = (x.K + 255) / 256;  // the last stage's box is zero-filled past K
         const int m_tile = 2 * x.pm + (int)rank;               // this CTA's 128 A rows
         const bool a_valid = m_tile * BM < x.M;
         const int nb_mine = 2 * x.pn + (int)rank;              // this CTA's 128 B rows
@@ -402,9 +395,18 @@ __device__ __forceinline__ void gemm_pairs(const Sched& sched, bool out_bf16, un
           if (b_valid) tma_load_pair(smem_u32(smem + OFF_B + s * B_BYTES), x.tmB, kt * BKB, nb_mine * 128, fb);
         }
       }
-      if (*abort_flag) {  // let copies already issued land before the CTA leaves
-        const unsigned long long t0 = now_ns();
-        while (now_ns() - t0 < 2000000ull) {
+      if (*abort_flag) {
+        // Copies already issued must land before the pair leaves.  They
+        // complete on the leader's full barriers, which the leader drains
+        // (bounded: a phase whose scale-warp arrivals were abandoned never
+        // completes); the peer cannot observe them and waits 2 ms instead.
+        if (leader) {
+          for (uint32_t i = it > STAGES ? it - STAGES : 0; i < it; ++i)
+            mbar_drain(full0 + 8 * (i % STAGES), (i / STAGES) & 1);
+        } else {
+          const unsigned long long t0 = now_ns();
+          while (now_ns() - t0 < 2000000ull) {
+          }
         }
       }
     }
@@ -422,7 +424,7 @@ __device__ __forceinline__ void gemm_pairs(const Sched& sched, bool out_bf16, un
       bool ok = true, next_ready = false;
       for (int t = first; t < num_tiles && ok; t += step, ++ti) {
         const Tile x = sched.get(t);
-        const int nk = x.K / 256;
+        const int nk = (x.K + 255) / 256, nkc = x.K / 64;
         if (!mbar_wait(accum_empty, (ti & 1) ^ 1, abort_flag, err)) break;
         tc_fence_after();
         for (int kt = 0; kt < nk; ++kt) {
@@ -434,9 +436,10 @@ __device__ __forceinline__ void gemm_pairs(const Sched& sched, bool out_bf16, un
           const uint32_t sn = s + 1 == STAGES ? 0 : s + 1, phn = s + 1 == STAGES ? ph ^ 1 : ph;
           const uint64_t da = da0 + (uint64_t)(s * (A_BYTES >> 4)), db = db0 + (uint64_t)(s * (B_BYTES >> 4));
           const uint32_t sfa = tmem + SFA_COL0 + 16 * s, sfb = tmem + SFB_COL0 + 32 * s;
+          const int kc = min(4, nkc - 4 * kt);  // K-steps of 64 in this stage (4 except at a K tail)
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            tc_mma_pair(tmem, da + 2 * j, db + 2 * j, sfa + 4 * j, sfb + 8 * j, (kt | j) != 0);
+            if (j < kc) tc_mma_pair(tmem, da + 2 * j, db + 2 * j, sfa + 4 * j, sfb + 8 * j, (kt | j) != 0);
             if (j == 2) next_ready = mbar_test(full0 + 8 * sn, phn);
           }
           tc_commit_pair(empty0 + 8 * s);
@@ -458,7 +461,7 @@ __device__ __forceinline__ void gemm_pairs(const Sched& sched, bool out_bf16, un
     bool ok = true;
     for (int t = first; t < num_tiles && ok; t += step) {
       const Tile x = sched.get(t);
-      const int nk = x.K / 256;
+      const int nk = (x.K + 255) / 256;
       for (int kt = 0; kt < nk; ++kt, ++it) {
         const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
         // warp vote: the tcgen05.st below is warp-collective
@@ -474,17 +477,8 @@ __device__ __forceinline__ void gemm_pairs(const Sched& sched, bool out_bf16, un
         for (int j = 0; j < 4; ++j) {
           const uint4 wa = sa[j * 32];
           va[4 * j] = wa.x; va[4 * j + 1] = wa.y; va[4 * j + 2] = wa.z; va[4 * j + 3] = wa.w;
-#if NVFP4_SFB_MODE == 0
           const uint4 w0 = sb[j * 32];        // B rows 0..127 of the tile
           const uint4 w1 = sb[128 + j * 32];  // B rows 128..255
-#elif NVFP4_SFB_MODE == 1
-          const uint4 w0 = sb[j * 32];        // own B rows at the first block position
-          const uint4 w1 = make_uint4(0, 0, 0, 0);
-#else
-          const uint4 own = sb[j * 32];       // own B rows at block position `rank`
-          const uint4 w0 = rank == 0 ? own : make_uint4(0, 0, 0, 0);
-          const uint4 w1 = rank == 0 ? make_uint4(0, 0, 0, 0) : own;
-#endif
           vb[8 * j] = w0.x; vb[8 * j + 1] = w0.y; vb[8 * j + 2] = w0.z; vb[8 * j + 3] = w0.w;
           vb[8 * j + 4] = w1.x; vb[8 * j + 5] = w1.y; vb[8 * j + 6] = w1.z; vb[8 * j + 7] = w1.w;
         }
@@ -502,36 +496,33 @@ __device__ __forceinline__ void gemm_pairs(const Sched& sched, bool out_bf16, un
       uint32_t it = 0;
       for (int t = first; t < num_tiles && !*abort_flag; t += step) {
         const Tile x = sched.get(t);
-        const int nk = x.K / 256;
-        const int64_t nka = x.K / 64;
+        const int nk = (x.K + 255) / 256;
+        const int nka = x.K / 64;  // 4-block scale atoms per 128 rows (K % 64 == 0)
         const int m_tile = 2 * x.pm + (int)rank;
         const bool a_valid = m_tile * BM < x.M;
-#if NVFP4_SFB_MODE == 0
-        const int sfb_blocks = min(2, (x.N - x.pn * BN) / 128);
+        // 128-row scale blocks of B that exist (the buffer is padded to 128 rows)
+        const int sfb_blocks = min(2, (x.N - x.pn * BN + 127) / 128);
         const int sfb_first = 2 * x.pn;
-#else
-        const int sfb_blocks = (2 * x.pn + (int)rank) * 128 < x.N ? 1 : 0;
-        const int sfb_first = 2 * x.pn + (int)rank;
-#endif
-        const uint32_t sf_tx = (a_valid ? SFA_BYTES : 0) + sfb_blocks * 2048;
         for (int kt = 0; kt < nk; ++kt, ++it) {
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
           if (!mbar_wait(empty0 + 8 * s, ph ^ 1, abort_flag, err)) break;
+          // the atoms of this stage's K-steps: 4, or fewer at a K tail (the
+          // next atoms in memory belong to the next 128 rows)
+          const uint32_t bytes = (uint32_t)min(4, nka - 4 * kt) * 512;
           const uint32_t sb = sff0 + 8 * s;
-          mbar_expect_tx(sb, sf_tx);
+          mbar_expect_tx(sb, (a_valid ? bytes : 0) + sfb_blocks * bytes);
           if (a_valid)
             bulk_g2s(smem_u32(smem + OFF_SFA + s * SFA_BYTES), x.sfa + ((int64_t)m_tile * nka + 4 * kt) * 512,
-                     SFA_BYTES, sb);
+                     bytes, sb);
           for (int nb = 0; nb < sfb_blocks; ++nb)
             bulk_g2s(smem_u32(smem + OFF_SFB + s * SFB_BYTES + nb * 2048),
-                     x.sfb + ((int64_t)(sfb_first + nb) * nka + 4 * kt) * 512, 2048, sb);
+                     x.sfb + ((int64_t)(sfb_first + nb) * nka + 4 * kt) * 512, bytes, sb);
         }
       }
-      if (*abort_flag) {  // let copies already issued land before the CTA leaves
-        const unsigned long long t0 = now_ns();
-        while (now_ns() - t0 < 2000000ull) {
-        }
-      }
+      // copies already issued land on this CTA's own scale barriers: drain
+      // the last round of every slot before the CTA leaves
+      if (*abort_flag)
+        for (uint32_t i = it > STAGES ? it - STAGES : 0; i < it; ++i) mbar_drain(sff0 + 8 * (i % STAGES), (i / STAGES) & 1);
     }
   } else {
     // ---------------- epilogue (each CTA: its 128 accumulator rows) ----------------
@@ -550,7 +541,12 @@ __device__ __forceinline__ void gemm_pairs(const Sched& sched, bool out_bf16, un
       const float alpha = __fmul_rn(*x.ga, *x.gb);
       const int col0 = x.pn * BN + half * 128;
       const int row0 = (2 * x.pm + (int)rank) * BM + q * 32;
-      const bool active = col0 < x.N && row0 < x.M;  // warp-uniform (M, N % 128 == 0)
+      // warp-uniform: this warp's 32 rows x 128 columns hold at least one
+      // output; stores of partial boxes are clipped by the tensor map, and
+      // boxes wholly past N are skipped
+      const bool active = col0 < x.N && row0 < x.M;
+      const int ncols = x.N - col0;           // valid columns of this warp's 128 (may exceed 128)
+      const bool row_ok = row0 + lane < x.M;  // this thread's row exists
       if (out_bf16) {
         uint32_t pk[64];
         if (active) {
@@ -578,10 +574,20 @@ __device__ __forceinline__ void gemm_pairs(const Sched& sched, bool out_bf16, un
         if (lane == 0) mbar_arrive_cluster(lead_accum_empty);
         if (amax_out && active) {
           // producer amax of the stored BF16 values: |x| bit patterns order
-          // like unsigned integers, two per word
+          // like unsigned integers, two per word (word i = columns 2i, 2i+1);
+          // elements outside M x N are left out
           uint32_t mx = 0;
+          if (ncols >= 128) {
 #pragma unroll
-          for (int i = 0; i < 64; ++i) mx = __vmaxu2(mx, pk[i] & 0x7FFF7FFFu);
+            for (int i = 0; i < 64; ++i) mx = __vmaxu2(mx, pk[i] & 0x7FFF7FFFu);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 64; ++i) {
+              const uint32_t keep = 2 * i + 1 < ncols ? 0x7FFF7FFFu : (2 * i < ncols ? 0x00007FFFu : 0u);
+              mx = __vmaxu2(mx, pk[i] & keep);
+            }
+          }
+          if (!row_ok) mx = 0;
           uint32_t m = max(mx & 0xFFFFu, mx >> 16) << 16;
           m = __reduce_max_sync(0xFFFFFFFFu, m);
           if (lane == 0 && m) atomicMax(amax_out, m);
@@ -589,6 +595,7 @@ __device__ __forceinline__ void gemm_pairs(const Sched& sched, bool out_bf16, un
         if (active) {
 #pragma unroll
           for (int cc = 0; cc < 2; ++cc) {  // 64 columns = one 128-byte box row
+            if (64 * cc >= ncols) break;
             if (lane == 0) bulk_wait_read0();
             __syncwarp();
 #pragma unroll
@@ -621,11 +628,13 @@ __device__ __forceinline__ void gemm_pairs(const Sched& sched, bool out_bf16, un
             uint32_t m = 0;
 #pragma unroll
             for (int i = 0; i < 32; ++i)
-              m = max(m, __float_as_uint(__fmul_rn(alpha, __uint_as_float(r[i]))) & 0x7FFFFFFFu);
+              if (32 * c + i < ncols)
+                m = max(m, __float_as_uint(__fmul_rn(alpha, __uint_as_float(r[i]))) & 0x7FFFFFFFu);
+            if (!row_ok) m = 0;
             m = __reduce_max_sync(0xFFFFFFFFu, m);
             if (lane == 0 && m) atomicMax(amax_out, m);
           }
-          if (active) {
+          if (active && 32 * c < ncols) {
             if (lane == 0) bulk_wait_read0();
             __syncwarp();
 #pragma unroll
@@ -672,25 +681,34 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_gemm_grouped(const __grid_co
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
+// Timeout word of the pipeline waits (one per device, shared by every GEMM
+// launched on it) and the slot that nvfp4_sync_check's exchange reads back.
 __device__ unsigned int g_device_error = 0;
+__device__ unsigned int g_device_error_taken = 0;
+
+__global__ void k_take_error() { g_device_error_taken = atomicExch(&g_device_error, 0u); }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
+  static std::atomic<EncodeTiledFn> cached{nullptr};
+  EncodeTiledFn fn = cached.load(std::memory_order_acquire);
   if (!fn) {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
+        q == cudaDriverEntryPointSuccess) {
       fn = reinterpret_cast<EncodeTiledFn>(p);
+      cached.store(fn, std::memory_order_release);
+    }
   }
   return fn;
 }
 
-// rows x (K/2) bytes, K-major, box = 128 B x 128 rows, 128B swizzle
+// rows x (K/2) bytes, K-major, box = 128 B x 128 rows, 128B swizzle.  Boxes
+// reaching past the last row or past K are zero-filled by the copy engine.
 bool make_code_map(CUtensorMap* m, const uint8_t* codes, int64_t rows, int64_t K) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
@@ -703,7 +721,8 @@ bool make_code_map(CUtensorMap* m, const uint8_t* codes, int64_t rows, int64_t K
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// D: rows x cols of bf16/fp32 with leading dimension ldd; box = 128 B x 32 rows, 128B swizzle
+// D: rows x cols of bf16/fp32 with leading dimension ldd; box = 128 B x 32 rows,
+// 128B swizzle.  Stores of boxes reaching past the tensor are clipped.
 bool make_out_map(CUtensorMap* m, void* d, int64_t rows, int64_t cols, int64_t ldd, bool bf16) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
@@ -717,24 +736,55 @@ bool make_out_map(CUtensorMap* m, void* d, int64_t rows, int64_t cols, int64_t l
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool smem_configured(const void* fn) {
-  return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) == cudaSuccess;
+// Per-device launch state.  Everything here depends on the device (symbol
+// addresses live in each device's context, the shared-memory opt-in is a
+// per-device function attribute), so it is cached per device ordinal;
+// concurrent first calls compute the same values, and the atomics make the
+// publication safe.
+constexpr int kMaxDevices = 64;
+enum KernelId { kSingle = 0, kGrouped = 1, kNumKernels = 2 };
+struct DeviceState {
+  std::atomic<unsigned int*> err{nullptr};
+  std::atomic<unsigned int*> err_taken{nullptr};
+  std::atomic<int> sms{0};
+  std::atomic<int> max_pairs[kNumKernels] = {};
+  std::atomic<bool> smem_ok[kNumKernels] = {};
+};
+DeviceState g_dev[kMaxDevices];
+
+DeviceState* device_state() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  return &g_dev[dev];
 }
 
-int num_sms() {
-  static int n = 0;
-  if (!n) {
+unsigned int* symbol_addr(const unsigned int& sym) {
+  void* q = nullptr;
+  return cudaGetSymbolAddress(&q, sym) == cudaSuccess ? reinterpret_cast<unsigned int*>(q) : nullptr;
+}
+
+int num_sms(DeviceState* st) {
+  int n = st->sms.load(std::memory_order_relaxed);
+  if (n <= 0) {
     int dev = 0;
     cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    st->sms.store(n, std::memory_order_relaxed);
   }
   return n;
 }
 
+bool smem_configured(DeviceState* st, KernelId k, const void* fn) {
+  if (st->smem_ok[k].load(std::memory_order_acquire)) return true;
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess) return false;
+  st->smem_ok[k].store(true, std::memory_order_release);
+  return true;
+}
+
 // grid of CTA pairs: one pair per two SMs, no more pairs than tiles
 template <class... Args>
-cudaError_t launch_pairs(void (*kernel)(Args...), int pair_tiles, int* max_pairs, cudaStream_t s, Args... args) {
+cudaError_t launch_pairs(void (*kernel)(Args...), int pair_tiles, DeviceState* st, KernelId k, cudaStream_t s,
+                         Args... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(NUM_THREADS, 1, 1);
   cfg.dynamicSmemBytes = SMEM_BYTES;
@@ -746,14 +796,16 @@ cudaError_t launch_pairs(void (*kernel)(Args...), int pair_tiles, int* max_pairs
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (*max_pairs == 0) {  // pairs that can be resident at once (clusters live inside one GPC)
-    cfg.gridDim = dim3(2 * (unsigned)(num_sms() / 2), 1, 1);
+  int max_pairs = st->max_pairs[k].load(std::memory_order_relaxed);
+  if (max_pairs <= 0) {  // pairs that can be resident at once (clusters live inside one GPC)
+    cfg.gridDim = dim3(2 * (unsigned)(num_sms(st) / 2), 1, 1);
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(kernel), &cfg) != cudaSuccess || n <= 0)
-      n = num_sms() / 2;
-    *max_pairs = n;
+      n = num_sms(st) / 2;
+    max_pairs = n;
+    st->max_pairs[k].store(n, std::memory_order_relaxed);
   }
-  const int pairs = pair_tiles < *max_pairs ? pair_tiles : *max_pairs;
+  const int pairs = pair_tiles < max_pairs ? pair_tiles : max_pairs;
   cfg.gridDim = dim3((unsigned)(2 * (pairs > 0 ? pairs : 1)), 1, 1);
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
@@ -761,12 +813,31 @@ cudaError_t launch_pairs(void (*kernel)(Args...), int pair_tiles, int* max_pairs
 }  // namespace
 
 unsigned int* device_error_word() {
-  static unsigned int* p = nullptr;
+  DeviceState* st = device_state();
+  if (!st) return nullptr;
+  unsigned int* p = st->err.load(std::memory_order_acquire);
   if (!p) {
-    void* q = nullptr;
-    if (cudaGetSymbolAddress(&q, g_device_error) == cudaSuccess) p = reinterpret_cast<unsigned int*>(q);
+    p = symbol_addr(g_device_error);
+    if (p) st->err.store(p, std::memory_order_release);
   }
   return p;
+}
+
+cudaError_t take_device_error(cudaStream_t s, unsigned int* value) {
+  DeviceState* st = device_state();
+  if (!st) return cudaErrorInvalidDevice;
+  unsigned int* p = st->err_taken.load(std::memory_order_acquire);
+  if (!p) {
+    p = symbol_addr(g_device_error_taken);
+    if (!p) return cudaErrorInvalidSymbol;
+    st->err_taken.store(p, std::memory_order_release);
+  }
+  k_take_error<<<1, 1, 0, s>>>();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = cudaMemcpyAsync(value, p, sizeof(unsigned int), cudaMemcpyDeviceToHost, s);
+  if (e != cudaSuccess) return e;
+  return cudaStreamSynchronize(s);
 }
 
 int gemm_tile_m() { return 2 * BM; }
@@ -780,78 +851,76 @@ cudaError_t launch_gemm(const GemmOperand& A, const GemmOperand& B, void* D, int
     *why = "cuTensorMapEncodeTiled failed (or driver entry point unavailable)";
     return cudaErrorInvalidValue;
   }
+  DeviceState* st = device_state();
   unsigned int* err = device_error_word();
-  if (!err) {
+  if (!st || !err) {
     *why = "device error word unavailable";
     return cudaErrorInvalidValue;
   }
-  static bool cfg = false;
-  if (!cfg) {
-    if (!smem_configured(reinterpret_cast<const void*>(k_gemm))) {
-      *why = "cudaFuncSetAttribute failed";
-      return cudaErrorInvalidValue;
-    }
-    cfg = true;
+  if (!smem_configured(st, kSingle, reinterpret_cast<const void*>(k_gemm))) {
+    *why = "cudaFuncSetAttribute failed";
+    return cudaErrorInvalidValue;
   }
   GemmArgs a{A.scales, B.scales, A.g, B.g, (int)A.rows, (int)B.rows, (int)A.K, out_bf16 ? 1 : 0, err,
              reinterpret_cast<unsigned int*>(amax_out)};
   const int tiles = (int)((A.rows + 2 * BM - 1) / (2 * BM)) * (int)((B.rows + BN - 1) / BN);
-  static int max_pairs = 0;
-  cudaError_t e = launch_pairs(k_gemm, tiles, &max_pairs, s, ta, tb, td, a);
+  cudaError_t e = launch_pairs(k_gemm, tiles, st, kSingle, s, ta, tb, td, a);
   if (e != cudaSuccess) *why = "cudaLaunchKernelEx (cluster of 2) failed";
   return e;
 }
 
 cudaError_t launch_gemm_grouped(int count, const GemmOperand* A, const GemmOperand* B, void* const* D, bool out_bf16,
                                 cudaStream_t s, const char** why) {
+  DeviceState* st = device_state();
   unsigned int* err = device_error_word();
-  if (!err) {
+  if (!st || !err) {
     *why = "device error word unavailable";
     return cudaErrorInvalidValue;
   }
-  static bool cfg = false;
-  if (!cfg) {
-    if (!smem_configured(reinterpret_cast<const void*>(k_gemm_grouped))) {
-      *why = "cudaFuncSetAttribute failed";
-      return cudaErrorInvalidValue;
-    }
-    cfg = true;
+  if (!smem_configured(st, kGrouped, reinterpret_cast<const void*>(k_gemm_grouped))) {
+    *why = "cudaFuncSetAttribute failed";
+    return cudaErrorInvalidValue;
   }
-  for (int base = 0; base < count; base += kGroupsPerLaunch) {
-    const int n = count - base < kGroupsPerLaunch ? count - base : kGroupsPerLaunch;
-    GroupedArgs g;
+  GroupedArgs g;
+  int n = 0, tiles = 0;
+  auto flush = [&]() -> cudaError_t {
+    if (n == 0) return cudaSuccess;
     g.count = n;
     g.out_bf16 = out_bf16 ? 1 : 0;
     g.err = err;
-    int tiles = 0;
-    for (int e = 0; e < n; ++e) {
-      const GemmOperand& a = A[base + e];
-      const GemmOperand& b = B[base + e];
-      if (!make_code_map(&g.tmA[e], a.codes, a.rows, a.K) || !make_code_map(&g.tmB[e], b.codes, b.rows, b.K) ||
-          !make_out_map(&g.tmD[e], D[base + e], a.rows, b.rows, b.rows, out_bf16)) {
-        *why = "cuTensorMapEncodeTiled failed (or driver entry point unavailable)";
-        return cudaErrorInvalidValue;
-      }
-      g.sfa[e] = a.scales;
-      g.sfb[e] = b.scales;
-      g.ga[e] = a.g;
-      g.gb[e] = b.g;
-      g.M[e] = (int)a.rows;
-      g.N[e] = (int)b.rows;
-      g.K[e] = (int)a.K;
-      g.tile_start[e] = tiles;
-      tiles += (int)((a.rows + 2 * BM - 1) / (2 * BM)) * (int)((b.rows + BN - 1) / BN);
-    }
     g.tile_start[n] = tiles;
-    if (tiles == 0) continue;
-    static int max_pairs = 0;
-    cudaError_t e = launch_pairs(k_gemm_grouped, tiles, &max_pairs, s, g);
-    if (e != cudaSuccess) {
-      *why = "cudaLaunchKernelEx (cluster of 2) failed";
-      return e;
+    const int t = tiles;
+    n = 0;
+    tiles = 0;
+    if (t == 0) return cudaSuccess;
+    cudaError_t e = launch_pairs(k_gemm_grouped, t, st, kGrouped, s, g);
+    if (e != cudaSuccess) *why = "cudaLaunchKernelEx (cluster of 2) failed";
+    return e;
+  };
+  for (int i = 0; i < count; ++i) {
+    const GemmOperand& a = A[i];
+    const GemmOperand& b = B[i];
+    if (a.rows == 0 || b.rows == 0) continue;  // an empty product: nothing to write
+    if (!make_code_map(&g.tmA[n], a.codes, a.rows, a.K) || !make_code_map(&g.tmB[n], b.codes, b.rows, b.K) ||
+        !make_out_map(&g.tmD[n], D[i], a.rows, b.rows, b.rows, out_bf16)) {
+      *why = "cuTensorMapEncodeTiled failed (or driver entry point unavailable)";
+      return cudaErrorInvalidValue;
+    }
+    g.sfa[n] = a.scales;
+    g.sfb[n] = b.scales;
+    g.ga[n] = a.g;
+    g.gb[n] = b.g;
+    g.M[n] = (int)a.rows;
+    g.N[n] = (int)b.rows;
+    g.K[n] = (int)a.K;
+    g.tile_start[n] = tiles;
+    tiles += (int)((a.rows + 2 * BM - 1) / (2 * BM)) * (int)((b.rows + BN - 1) / BN);
+    if (++n == kGroupsPerLaunch) {
+      cudaError_t e = flush();
+      if (e != cudaSuccess) return e;
     }
   }
-  return cudaSuccess;
+  return flush();
 }
 
 }  // namespace nvfp4

@@ -43,6 +43,9 @@ struct GroupedArgs {
 };
 
 unsigned int* device_error_word();
+// Read and clear the current device's timeout word in one atomic exchange
+// (ordered on `s`), then synchronise `s` and return the value read.
+cudaError_t take_device_error(cudaStream_t s, unsigned int* value);
 int gemm_tile_m();
 int gemm_tile_n();
 cudaError_t launch_gemm(const GemmOperand& A, const GemmOperand& B, void* D, int64_t ldd, bool out_bf16, cudaStream_t s,

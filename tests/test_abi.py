@@ -95,9 +95,13 @@ def test_gemm_argument_errors(L):
     B = _fake_tensor(256, 256, base=0x800000)
     D = ctypes.c_void_p(0x4000000)
     assert L.nvfp4_gemm(ctypes.byref(A), ctypes.byref(_fake_tensor(256, 512)), D, nv.BF16, 256, None) == 1
-    assert L.nvfp4_gemm(ctypes.byref(_fake_tensor(128, 128)), ctypes.byref(_fake_tensor(256, 128)), D, nv.BF16,
+    # K must be a multiple of 64; M and N may be anything
+    assert L.nvfp4_gemm(ctypes.byref(_fake_tensor(128, 96)), ctypes.byref(_fake_tensor(256, 96)), D, nv.BF16,
                         256, None) == 2
-    assert L.nvfp4_gemm(ctypes.byref(_fake_tensor(100, 256)), ctypes.byref(B), D, nv.BF16, 256, None) == 2
+    assert "multiple of 64" in L.nvfp4_last_error().decode()
+    # N * elsize must keep rows of D 16-byte aligned (ldd = N = 100 BF16: 200 bytes)
+    assert L.nvfp4_gemm(ctypes.byref(_fake_tensor(100, 256)), ctypes.byref(_fake_tensor(100, 256, base=0x800000)), D,
+                        nv.BF16, 100, None) == 3
     assert L.nvfp4_gemm(ctypes.byref(A), ctypes.byref(B), D, nv.BF16, 200, None) == 1       # ldd < N
     assert L.nvfp4_gemm(ctypes.byref(A), ctypes.byref(B), ctypes.c_void_p(0x4000008), nv.BF16, 256, None) == 3
     assert L.nvfp4_gemm(ctypes.byref(A), ctypes.byref(B), D, 9, 256, None) == 1

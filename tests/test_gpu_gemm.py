@@ -266,3 +266,83 @@ def test_llama405b_full_size_sampled():
     ref, bound = oracle.gemm_reference(refs["X"], refs["W"])
     got = d[torch.from_numpy(rx).cuda()][:, torch.from_numpy(rw).cuda()].float().cpu().numpy()
     gemm_check(got, ref, bound, True, "405B fprop")
+
+
+# ---------------------------------------------------------------------------
+# Shapes off the 128 x 128 x 256 tile grid: any M and N, K % 64 == 0.  The
+# output sits inside a larger buffer (ldd > N, extra rows) filled with a
+# sentinel, which must survive: the clipped stores write only M x N.
+# ---------------------------------------------------------------------------
+RAGGED = [(200, 72, 320), (1, 128, 256), (130, 1000, 64), (257, 136, 192), (129, 264, 448), (3, 8, 128),
+          (384, 520, 832)]
+
+
+def _ragged_operands(M, N, K, seed):
+    a = torch.from_numpy(synthetic.normal((M, K), 1.0, seed)).to(torch.bfloat16)
+    b = torch.from_numpy(synthetic.normal((N, K), 0.02, seed + 1)).to(torch.bfloat16)
+    qa, ra = quantize_both(a)
+    qb, rb = quantize_both(b, block="2d" if N % 16 == 0 else "1d")
+    return qa, ra, qb, rb
+
+
+@pytest.mark.parametrize("M,N,K", RAGGED)
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_gemm_ragged_shapes(M, N, K, out_dtype):
+    qa, ra, qb, rb = _ragged_operands(M, N, K, 7 * M + N + K)
+    pad = 16 // (2 if out_dtype == torch.bfloat16 else 4)
+    big = torch.full((M + 5, N + pad), -7.0, dtype=out_dtype, device="cuda")
+    nv.gemm(qa, qb, out=big[:M, :N])
+    nv.sync_check()
+    full = big.float().cpu().numpy()
+    ref, bound = oracle.gemm_reference(ra, rb)
+    gemm_check(full[:M, :N], ref, bound, out_dtype == torch.bfloat16, f"{M}x{N}x{K}")
+    assert (full[:M, N:] == -7.0).all(), "write past N"
+    assert (full[M:] == -7.0).all(), "write past M"
+
+
+@pytest.mark.parametrize("M,N,K", [(200, 72, 320), (130, 1000, 64), (1, 128, 256)])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_gemm_amax_ragged(M, N, K, out_dtype):
+    """The producer amax covers exactly the M x N stored values."""
+    qa, ra, qb, rb = _ragged_operands(M, N, K, 11 * M + N + K)
+    d, amax = nv.gemm_amax(qa, qb, out_dtype=out_dtype)
+    nv.sync_check()
+    assert float(amax.cpu()[0]) == float(d.float().abs().max().cpu())
+
+
+def test_gemm_k_zero_writes_zeros():
+    a, b = nv.NVFP4Tensor.empty(40, 0), nv.NVFP4Tensor.empty(24, 0)
+    for t in (a, b):
+        t.global_scale.fill_(1.0)
+    big = torch.full((40, 32), -7.0, dtype=torch.float32, device="cuda")
+    nv.gemm(a, b, out=big[:, :24])
+    nv.sync_check()
+    full = big.cpu().numpy()
+    assert (full[:, :24] == 0).all() and (full[:, 24:] == -7.0).all()
+
+
+def test_gemm_grouped_ragged_experts():
+    """Routed experts with token counts that are not multiples of 128 (and one
+    expert with no tokens), as MoE routing produces."""
+    Ms = [1, 130, 0, 200, 512, 77, 384, 5]
+    N, K = 136, 320
+    qa, qb, ra, rb = [], [], [], []
+    for e, M in enumerate(Ms):
+        b = torch.from_numpy(synthetic.normal((N, K), 0.02, 300 + e)).to(torch.bfloat16)
+        y, yr = quantize_both(b)
+        qb.append(y); rb.append(yr)
+        if M == 0:
+            qa.append(nv.NVFP4Tensor.empty(0, K)); ra.append(None)
+            qa[-1].global_scale.fill_(1.0)
+            continue
+        a = torch.from_numpy(synthetic.normal((M, K), 1.0, 400 + e)).to(torch.bfloat16)
+        x, xr = quantize_both(a)
+        qa.append(x); ra.append(xr)
+    outs = [torch.full((M, N), -7.0, dtype=torch.bfloat16, device="cuda") for M in Ms]
+    nv.gemm_grouped(qa, qb, out_dtype=torch.bfloat16, out=outs)
+    nv.sync_check()
+    for e, M in enumerate(Ms):
+        if M == 0:
+            continue
+        ref, bound = oracle.gemm_reference(ra[e], rb[e])
+        gemm_check(outs[e].float().cpu().numpy(), ref, bound, True, f"expert {e} (M={M})")
