@@ -834,107 +834,179 @@ def _oracle_inputs(workload: str):
     return wl.tensors["X"].to(torch.float32).numpy(), wl.tensors["W"].to(torch.float32).numpy()
 
 
-def _oracle_sample(workload: str, X, W, rx: int, rw: int, rg: int):
-    """Time the oracle on a slice of the step and return (time scaled to one
-    whole step, seconds spent).  Fprop-shaped workloads: rows [0, rx) of X
-    (1D), [0, rw) of W (2D), rg GEMM output rows against those rw columns.
-    Wgrad: the first rx columns of dY and rw columns of X (their transposed,
-    RHT, quantization), rg output rows.  MoE: one expert, rg output rows."""
-    import oracle
-    c = WORKLOADS[workload]
-    M, N = c["M"], c["N"]
-    if workload == "w4a16":   # rw weight rows (quantized outside the timing); scaled to N rows and L layers
-        qw = oracle.quantize(W[:rw], block2d=True)
-        t0 = time.perf_counter()
-        oracle.w4a16_reference(X, qw)
-        t1 = time.perf_counter()
-        return c["L"] * (t1 - t0) * N / rw, t1 - t0
-    if workload == "moe":   # one expert: W^T with Four-over-Six, X max-6; scaled to E experts
-        E, Mt = c["E"], c["M"]
-        t0 = time.perf_counter()
-        qw = oracle.quantize(W, transpose=True, four_over_six=True)
-        qx = oracle.quantize(X)
-        t1 = time.perf_counter()
-        oracle.gemm_reference(qx, qw, rows=np.arange(rg))
-        t2 = time.perf_counter()
-        return E * ((t1 - t0) + (t2 - t1) * Mt / rg), t2 - t0
-    t0 = time.perf_counter()
-    if workload == "wgrad":   # output rows = columns of the inputs
-        qa = oracle.quantize(np.ascontiguousarray(X[:, :rx]), transpose=True, rht=True, stochastic=True, seed=1,
-                             rht_seed=1)
-        t1 = time.perf_counter()
-        qb = oracle.quantize(np.ascontiguousarray(W[:, :rw]), transpose=True, rht=True, rht_seed=1)
-        sa, sb = M / rx, N / rw
-    else:
-        qa = oracle.quantize(X[:rx])
-        t1 = time.perf_counter()
-        qb = oracle.quantize(W[:rw], block2d=workload != "pr1")
-        sa, sb = M / rx, N / rw
-    t2 = time.perf_counter()
-    g = min(rg, qa.R)
-    oracle.gemm_reference(qa, qb, rows=np.arange(g))
-    t3 = time.perf_counter()
-    return (t1 - t0) * sa + (t2 - t1) * sb + (t3 - t2) * (M / g) * sb, t3 - t0
-
-
 def _flops(workload: str) -> float:
     c = WORKLOADS[workload]
     return 2.0 * c.get("E", 1) * c.get("L", 1) * c["M"] * c["N"] * c["K"]
 
 
-# per workload: the slice the oracle is timed on (see _oracle_sample), as (rx, rw, rg)
-_CPU_SAMPLE = {"pr1": (256, 256, 256), "llama8b": (8192, 14336, 2048), "llama405b": (2048, 4096, 256),
-               "wgrad": (2048, 1024, 512), "moe": (0, 0, 256), "w4a16": (0, 14336, 0)}
-_REF_SAMPLE = {"pr1": (256, 256, 64), "llama8b": (512, 896, 64), "llama405b": (128, 256, 16),
-               "wgrad": (256, 64, 64), "moe": (0, 0, 16), "w4a16": (0, 2048, 0)}
+def _linear_fit(n1: int, t1: float, n2: int, t2: float):
+    """t(n) = a + b * n through two timed sizes: (fixed seconds, seconds per unit)."""
+    b = max((t2 - t1) / (n2 - n1), 0.0)
+    return max(t1 - b * n1, 0.0), b
 
 
-def _sample_desc(workload: str, rx: int, rw: int, rg: int) -> str:
+# Per workload, the slices the oracle is timed on: (X rows, W rows, GEMM output rows), each part timed at that
+# size and at twice it.  Fprop: rows of X (1D) and of W (2D); the GEMM reference runs those output rows against
+# the W slice.  Wgrad: columns of dY and of X (transposed RHT quantization).  The 1-core figure uses the
+# sizes divided by _ONE_CORE_DIV.
+_ORACLE_SLICES = {"llama8b": (2048, 3584, 512), "llama405b": (512, 1024, 256), "wgrad": (1024, 512, 512),
+                  "pr1": (128, 128, 128)}
+_ONE_CORE_DIV = 8
+
+
+def _time(fn):
+    t0 = time.perf_counter()
+    r = fn()
+    return time.perf_counter() - t0, r
+
+
+def _oracle_step(workload: str, X, W, div: int = 1) -> dict:
+    """Time the oracle, as it stands, on bounded slices of one step and
+    extrapolate each part linearly to the whole step.
+
+    Each part (quantize X, quantize W, the fp64 GEMM reference) is timed at
+    two sizes n and 2n; t(n) = a + b*n separates the fixed cost a (charged
+    once per step) from the per-unit cost b, so the extrapolation never
+    multiplies a fixed cost.  The GEMM part runs its output rows against the
+    2n-row W slice and is scaled by N / (that slice).  MoE times one whole
+    expert (scaled to 64), W4A16 one whole layer (scaled to 8): both are the
+    step's own repeated unit.  Returns the extrapolated step seconds, the
+    seconds actually spent, and the per-part fits."""
+    import oracle
+    c = WORKLOADS[workload]
+    M, N = c["M"], c["N"]
     if workload == "w4a16":
-        return (f"w4a16: oracle W4A16 product (BF16-rounded decode, fp64 matmul) of the {WORKLOADS['w4a16']['M']} "
-                f"tokens with {rw} weight rows (quantized outside the timing), scaled to all rows and "
-                f"{WORKLOADS['w4a16']['L']} layers")
-    return (f"{workload}: oracle quantize of a slice (rx={rx}, rw={rw}) and fp64 GEMM of {rg} output rows, "
-            "each part scaled to the whole step (MoE: one expert, scaled to 64)")
+        qw = oracle.quantize(W, block2d=True)      # quantized once, outside the step (as on the GPU)
+        t, _ = _time(lambda: oracle.w4a16_reference(X, qw))
+        return {"step_s": c["L"] * t, "spent_s": t, "parts": {"w4a16_layer_s": round(t, 4)},
+                "work": f"one whole layer (W {N}x{c['K']}, {c['M']} tokens), x{c['L']} layers"}
+    if workload == "moe":
+        tw, qw = _time(lambda: oracle.quantize(W, transpose=True, four_over_six=True))
+        tx, qx = _time(lambda: oracle.quantize(X))
+        tg, _ = _time(lambda: oracle.gemm_reference(qx, qw))
+        t = tw + tx + tg
+        return {"step_s": c["E"] * t, "spent_s": t,
+                "parts": {"quantize_w_s": round(tw, 4), "quantize_x_s": round(tx, 4), "gemm_s": round(tg, 4)},
+                "work": f"one whole expert (W_e^T Four-over-Six, X_e, GEMM {c['M']}x{N}x{c['K']}), x{c['E']}"}
+    rx, rw, rg = (max(1, v // div) for v in _ORACLE_SLICES[workload])
+    if workload == "pr1":   # the whole step is small: time it as it is
+        tq1, qa = _time(lambda: oracle.quantize(X))
+        tq2, qb = _time(lambda: oracle.quantize(W))
+        tg, _ = _time(lambda: oracle.gemm_reference(qa, qb))
+        t = tq1 + tq2 + tg
+        return {"step_s": t, "spent_s": t, "parts": {"quantize_a_s": tq1, "quantize_b_s": tq2, "gemm_s": tg},
+                "work": "the whole step (no extrapolation)"}
+    if workload == "wgrad":
+        qa_fn = lambda n: oracle.quantize(np.ascontiguousarray(X[:, :n]), transpose=True, rht=True, stochastic=True,
+                                          seed=1, rht_seed=1)
+        qb_fn = lambda n: oracle.quantize(np.ascontiguousarray(W[:, :n]), transpose=True, rht=True, rht_seed=1)
+    else:
+        qa_fn = lambda n: oracle.quantize(X[:n])
+        qb_fn = lambda n: oracle.quantize(W[:n], block2d=True)
+    spent = 0.0
+    fits = {}
+    ta1, _ = _time(lambda: qa_fn(rx))
+    ta2, qa = _time(lambda: qa_fn(2 * rx))
+    tb1, _ = _time(lambda: qb_fn(rw))
+    tb2, qb = _time(lambda: qb_fn(2 * rw))
+    tg1, _ = _time(lambda: oracle.gemm_reference(qa, qb, rows=np.arange(rg)))
+    tg2, _ = _time(lambda: oracle.gemm_reference(qa, qb, rows=np.arange(2 * rg)))
+    spent = ta1 + ta2 + tb1 + tb2 + tg1 + tg2
+    fa, fb, fg = _linear_fit(rx, ta1, 2 * rx, ta2), _linear_fit(rw, tb1, 2 * rw, tb2), _linear_fit(rg, tg1, 2 * rg, tg2)
+    step = (fa[0] + fa[1] * M) + (fb[0] + fb[1] * N) + (fg[0] + fg[1] * M) * (N / (2 * rw))
+    for name, (a, b), n, t in (("quantize_a", fa, rx, ta1), ("quantize_b", fb, rw, tb1), ("gemm", fg, rg, tg1)):
+        fits[name] = {"fixed_s": round(a, 5), "per_unit_us": round(b * 1e6, 4), "fixed_frac_at_n": round(a / t, 4)}
+    unit = "columns" if workload == "wgrad" else "rows"
+    return {"step_s": step, "spent_s": spent, "parts": fits,
+            "work": (f"quantize A {unit} [0,{rx}) and [0,{2 * rx}), B {unit} [0,{rw}) and [0,{2 * rw}), fp64 GEMM of "
+                     f"{rg} and {2 * rg} output rows x {2 * rw} columns; each part fit as a + b*n and extrapolated "
+                     f"to the whole step")}
+
+
+def _set_threads(n: int | None):
+    """Threads of the oracle's OpenMP loops and of numpy's BLAS (None: all)."""
+    import ctypes
+    try:
+        ctypes.CDLL("libgomp.so.1").omp_set_num_threads(n or len(os.sched_getaffinity(0)))
+    except OSError:
+        pass
+    try:
+        from threadpoolctl import threadpool_limits
+        return threadpool_limits(limits=n)
+    except ImportError:
+        return None
 
 
 def cpu_baseline(workload: str):
-    """The oracle as it stands on the host cores, on a bounded sample of one
-    step (a few seconds of CPU work), scaled to the whole step."""
+    """The oracle as it stands on the host cores: all cores, then one core on
+    slices 1/8 the size, each extrapolated to one whole step (labelled)."""
     import oracle
     oracle.build()
     X, W = _oracle_inputs(workload)
-    rx, rw, rg = _CPU_SAMPLE[workload]
-    t_step, spent = _oracle_sample(workload, X, W, rx, rw, rg)
-    return {"value": round(_flops(workload) / t_step / 1e12, 6), "unit": "TFLOP/s",
-            "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
-            "sample": _sample_desc(workload, rx, rw, rg),
-            "sample_seconds": round(spent, 2), "extrapolated_step_seconds": round(t_step, 2)}
+    cores = len(os.sched_getaffinity(0))
+    _set_threads(None)
+    r = _oracle_step(workload, X, W)
+    r1 = None
+    if workload in _ORACLE_SLICES:   # MoE and W4A16 time a whole expert / layer: no 1-core run of that size
+        lim = _set_threads(1)
+        r1 = _oracle_step(workload, X, W, div=1 if workload == "pr1" else _ONE_CORE_DIV)
+        if lim is not None:
+            lim.restore_original_limits()
+        _set_threads(None)
+    flops = _flops(workload)
+    out = {"value": round(flops / r["step_s"] / 1e12, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+           "sample": r["work"], "extrapolated": workload != "pr1",
+           "extrapolated_step_seconds": round(r["step_s"], 3), "sample_seconds": round(r["spent_s"], 2),
+           "parts": r["parts"]}
+    if r1 is not None:
+        out["one_core"] = {"value": round(flops / r1["step_s"] / 1e12, 6), "cores": 1,
+                           "extrapolated_step_seconds": round(r1["step_s"], 3),
+                           "sample_seconds": round(r1["spent_s"], 2), "sample": r1["work"]}
+    return out
 
 
 def run_reference(args):
     """The base contract's reference arm for a method with no installable
-    code: the oracle, timed on the host cores, each step a bounded sample of
-    the workload (inputs generated once, outside the timing)."""
+    code: the oracle, timed on the host cores.  Each step runs the same
+    bounded sample as the cpu_baseline key and extrapolates it to the whole
+    step with the same model; ms_per_step is the time the sample took."""
     import oracle
     oracle.build()
+    _set_threads(None)
     X, W = _oracle_inputs(args.workload)
-    rx, rw, rg = _REF_SAMPLE[args.workload]
-    sample = "per step: " + _sample_desc(args.workload, rx, rw, rg)
     for _ in range(args.warmup):
-        _oracle_sample(args.workload, X, W, rx, rw, rg)
-    t_steps = [_oracle_sample(args.workload, X, W, rx, rw, rg)[0] for _ in range(max(1, args.steps))]
-    t = statistics.mean(t_steps)
-    value = _flops(args.workload) / t / 1e12
+        _oracle_step(args.workload, X, W)
+    runs = [_oracle_step(args.workload, X, W) for _ in range(max(1, args.steps))]
+    t_full = statistics.mean(r["step_s"] for r in runs)
+    t_sample = statistics.mean(r["spent_s"] for r in runs)
+    value = _flops(args.workload) / t_full / 1e12
     c = WORKLOADS[args.workload]
     cfg = {"workload": args.workload, **{k: v for k, v in c.items() if k != "desc"}, "desc": c["desc"]}
+    cores = len(os.sched_getaffinity(0))
     return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t * 1e3, 1), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "fp32/fp64 (CPU oracle)", "data": "synthetic",
-            "config": cfg,
-            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": len(os.sched_getaffinity(0)),
-                             "kind": "oracle", "sample": sample},
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_sample * 1e3, 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp32/fp64 (CPU oracle)",
+            "data": "synthetic", "config": cfg,
+            "value_is": ("2*M*N*K / the whole step's oracle time, extrapolated from the timed sample (each part fit "
+                         "as a + b*n at two sizes); ms_per_step is the time the sample itself took"),
+            "extrapolated_step_ms": round(t_full * 1e3, 1),
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": "per step: " + runs[0]["work"], "extrapolated": args.workload != "pr1"},
             "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def run_oracle_full_gemm():
+    """One-off: the oracle's fp64 GEMM reference of the whole Llama-3-8B fprop
+    (8192 x 14336 x 4096) on the host cores, with its wall time."""
+    import oracle
+    oracle.build()
+    _set_threads(None)
+    X, W = _oracle_inputs("llama8b")
+    tq, (qa, qb) = _time(lambda: (oracle.quantize(X), oracle.quantize(W, block2d=True)))
+    tg, _ = _time(lambda: oracle.gemm_reference(qa, qb))
+    return {"oracle_full_gemm": "llama8b", "M": 8192, "N": 14336, "K": 4096, "cores": len(os.sched_getaffinity(0)),
+            "quantize_both_s": round(tq, 2), "gemm_reference_s": round(tg, 2),
+            "gemm_tflops_fp64": round(2 * 8192 * 14336 * 4096 / tg / 1e12, 4)}
 
 
 def main():
@@ -945,7 +1017,12 @@ def main():
     ap.add_argument("--workload", default="llama8b", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--oracle-full-gemm", action="store_true",
+                    help="time the oracle's full Llama-3-8B fp64 GEMM once on the host cores and exit")
     args = ap.parse_args()
+    if args.oracle_full_gemm:
+        print(json.dumps(run_oracle_full_gemm()), flush=True)
+        return
     if args.warmup < 3:
         args.warmup = 3
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -126,25 +126,106 @@ __device__ __forceinline__ uint32_t rht_sign_mask(uint64_t rht_seed) {
   return w.x & 0xFFFFu;
 }
 
-// v <- 1/4 * H16 * diag(sigma) * v, fast Walsh-Hadamard butterfly in fp32
-// (Sylvester order), then the exact 1/4.
-__device__ __forceinline__ void rht16(float v[16], uint32_t sign_mask) {
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = ((sign_mask >> i) & 1u) ? -v[i] : v[i];
+// Packed fp32x2 multiply, each lane an IEEE round-to-nearest-even product
+// with subnormals kept (PTX with an explicit rounding mode).  Used only where
+// the product feeds a conversion, never an addition, so no fused
+// multiply-add can form from it.
+__device__ __forceinline__ float2 mul2_rn(float2 a, float2 b) {
+  float2 r;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+// Packed fp32x2 IEEE arithmetic (round to nearest even per lane).
+__device__ __forceinline__ float2 add2_rn(float2 a, float2 b) {
+  float2 r;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(r.x), "=f"(r.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+__device__ __forceinline__ float2 sub2_rn(float2 a, float2 b) {
+  float2 r;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "sub.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(r.x), "=f"(r.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+// a * b + c with one rounding per lane
+__device__ __forceinline__ float2 fma2_rn(float2 a, float2 b, float2 c) {
+  float2 r;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(r.x), "=f"(r.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return r;
+}
+
+// In-place 16-point Walsh-Hadamard butterfly (Sylvester order) on two
+// vectors at once (lanes .x and .y).
+__device__ __forceinline__ void wht16x2(float2 v[16]) {
 #pragma unroll
   for (int h = 1; h < 16; h <<= 1) {
 #pragma unroll
     for (int i = 0; i < 16; i += 2 * h) {
 #pragma unroll
       for (int j = i; j < i + h; ++j) {
-        float a = v[j], b = v[j + h];
-        v[j] = __fadd_rn(a, b);
-        v[j + h] = __fsub_rn(a, b);
+        const float2 a = v[j], b = v[j + h];
+        v[j] = add2_rn(a, b);
+        v[j + h] = sub2_rn(a, b);
       }
     }
   }
+}
+
+// Split constant of a chunk whose largest magnitude is m (finite, below
+// 2^124): c = 1.5 * 2^(E+4), E the binary exponent of m.  For |x| <= m,
+// x + c stays in c's binade, whose spacing is 2^(E-19).
+__device__ __forceinline__ float rht_split_const(float m) {
+  return __uint_as_float(((((__float_as_uint(m) >> 23) & 0xFFu) + 4u) << 23) | 0x400000u);
+}
+
+// v[h] <- 1/4 * H16 * diag(sigma) * v[h] for the two 16-element chunks h = 0, 1,
+// correctly rounded: every result is the fp32 value nearest the exact one.
+//   Each input is split exactly as x = hi + lo, hi = x rounded to a multiple
+//   of 2^(E-19) (E the exponent of the chunk's largest |x|, through
+//   t = fl(sigma*x + c), c = 1.5 * 2^(E+4)), lo = sigma*x - hi.  hi has at most
+//   20 significant bits below 2^(E+1), so every partial sum of its butterfly
+//   (below 2^(E+5), a multiple of 2^(E-19)) is an fp32 value: the butterfly of
+//   hi is exact.  |lo| <= 2^(E-20), and lo keeps the bits of x below the hi
+//   grid, so the butterfly of lo is exact whenever the chunk's smallest
+//   nonzero |x| is within 2^-33 (BF16 input) or 2^-17 (FP32 input) of its
+//   largest.  The result is then fl(1/4 * Ylo + 1/4 * Yhi), one rounding of
+//   the exact value.  (Outside that range the lo butterfly rounds at 2^-40
+//   of the chunk maximum.)  The sign diagonal rides in the first fma.
+__device__ __forceinline__ void rht16x2(float v[2][16], uint32_t sign_mask) {
+  float m0 = 0.0f, m1 = 0.0f;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __fmul_rn(v[i], 0.25f);
+  for (int i = 0; i < 16; ++i) {
+    m0 = fmaxf(m0, fabsf(v[0][i]));
+    m1 = fmaxf(m1, fabsf(v[1][i]));
+  }
+  const float2 c = make_float2(rht_split_const(m0), rht_split_const(m1));
+  float2 nh[16], lo[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float sg = ((sign_mask >> i) & 1u) ? -1.0f : 1.0f;
+    const float2 x = make_float2(v[0][i], v[1][i]), sgn = make_float2(sg, sg);
+    const float2 t = fma2_rn(x, sgn, c);  // fl(sigma*x + c)
+    nh[i] = sub2_rn(c, t);                // -hi, exact (t and c share a binade)
+    lo[i] = fma2_rn(x, sgn, nh[i]);       // sigma*x - hi, exact
+  }
+  wht16x2(nh);
+  wht16x2(lo);
+  const float2 q = make_float2(0.25f, 0.25f), nq = make_float2(-0.25f, -0.25f);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float2 y = fma2_rn(lo[i], q, mul2_rn(nh[i], nq));  // one rounding of (Ylo + Yhi) / 4
+    v[0][i] = y.x;
+    v[1][i] = y.y;
+  }
 }
 
 // --------------------------------------------------------------------------
@@ -170,19 +251,6 @@ __device__ __forceinline__ uint32_t block_scale(float amax_b, float mg, float g,
   return b;
 }
 
-// Packed fp32x2 multiply, each lane an IEEE round-to-nearest-even product
-// with subnormals kept (PTX with an explicit rounding mode).  Used only where
-// the product feeds a conversion, never an addition, so no fused
-// multiply-add can form from it.
-__device__ __forceinline__ float2 mul2_rn(float2 a, float2 b) {
-  float2 r;
-  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
-      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
-      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-      : "=f"(r.x), "=f"(r.y)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-  return r;
-}
 // Encode 16 values with block reciprocal rcp into two 32-bit words of codes.
 // The products are paired into packed fp32x2 multiplies (each lane an IEEE
 // round-to-nearest product, the same value as a scalar multiply).

@@ -302,8 +302,8 @@ __device__ __forceinline__ void quant_rows_body(const Src& src, const QuantArgs&
       r[h] = ref.ty * 128 + rl + 64 * h;
       valid[h] = r[h] < R && kb < KB;
       cur[h].unpack(v[h]);
-      if constexpr (RHT) rht16(v[h], mask);
     }
+    if constexpr (RHT) rht16x2(v, mask);
     if constexpr (AMAX_ONLY) {
       run_max = fmaxf(run_max, fmaxf(absmax16(v[0]), absmax16(v[1])));
     } else {
@@ -501,10 +501,7 @@ __device__ __forceinline__ void quant_cols_body(const Src& src, const QuantArgs&
     float v[2][16];
 #pragma unroll
     for (int e = 0; e < 16; ++e) ColTile<T>::pair(tile_s, 16 * kbl + e, np, v[0][e], v[1][e]);
-    if constexpr (RHT) {
-      rht16(v[0], mask);
-      rht16(v[1], mask);
-    }
+    if constexpr (RHT) rht16x2(v, mask);
     bool valid[2];
 #pragma unroll
     for (int h = 0; h < 2; ++h) valid[h] = (n0 + 2 * np + h < N) && kb < KB;

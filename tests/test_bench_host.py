@@ -28,8 +28,23 @@ def test_flop_counts():
     assert bench._flops("w4a16") == 2.0 * w["w4a16"]["L"] * w["w4a16"]["M"] * 14336 * 4096
 
 
-def test_every_workload_has_a_sample_and_a_description():
+def test_every_workload_has_an_oracle_sample():
     for name, c in bench.WORKLOADS.items():
         assert c["desc"]
-        assert name in bench._CPU_SAMPLE and name in bench._REF_SAMPLE
-        assert bench._sample_desc(name, *bench._CPU_SAMPLE[name])
+        assert name in bench._ORACLE_SLICES or name in ("moe", "w4a16")
+
+
+def test_linear_fit_separates_fixed_cost():
+    """t(n) = a + b*n from two sizes: the fixed part is recovered, so the
+    extrapolation to a large n does not multiply it."""
+    a, b = bench._linear_fit(100, 1.0 + 0.01 * 100, 200, 1.0 + 0.01 * 200)
+    assert abs(a - 1.0) < 1e-12 and abs(b - 0.01) < 1e-12
+    assert bench._linear_fit(10, 2.0, 20, 1.9) == (2.0, 0.0)   # noise never gives a negative slope
+
+
+def test_oracle_step_pr1_runs_whole_step():
+    import oracle
+    oracle.build()
+    X, W = bench._oracle_inputs("pr1")
+    r = bench._oracle_step("pr1", X, W)
+    assert r["step_s"] == r["spent_s"] > 0 and "no extrapolation" in r["work"]
