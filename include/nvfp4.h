@@ -257,6 +257,33 @@ nvfp4_status nvfp4_gemm_amax(const nvfp4_tensor* A, const nvfp4_tensor* B, void*
                              float* amax_out, void* stream);
 
 /*
+ * nvfp4_gemm_quantize - the GEMM whose epilogue also emits the next layer's
+ * NVFP4 input: D is rounded to BF16 exactly as nvfp4_gemm with dt = BF16
+ * writes it, and that M x N BF16 matrix is quantized with 1D blocks of 16
+ * along N, round to nearest even, max-6 scaling, using the tensor amax
+ * *amax_in (the "producer amax" of "NVIDIA Introduces a 4-Bit Pretraining
+ * Methodology Using NVFP4": typically the previous step's amax_out, or a
+ * bound the caller holds).  `out` then equals
+ *   nvfp4_quantize(D_bf16, BF16, M, N, N, {1D, RNE, max-6, transpose 0},
+ *                  amax_in, out)
+ * bit for bit, without D being written or read back.  D's codes and scales
+ * are written for exactly the M x N outputs (scale padding as 0), and
+ * out->global_scale and out->amax are set from *amax_in.  Values above
+ * *amax_in saturate to the format's maximum, as in nvfp4_quantize.
+ *   A, B     as nvfp4_gemm (K % 64 == 0, K > 0).
+ *   amax_in  device float[1], read.
+ *   D        device BF16 [M][ldd] or NULL (the BF16 output is then not
+ *            stored); ldd >= N, ldd % 8 == 0, 16-byte aligned.
+ *   amax_out device float[1] or NULL: as nvfp4_gemm_amax, max |D_bf16| over
+ *            the outputs, for the next step's amax_in.  Must not alias
+ *            amax_in or out->amax.
+ *   out      host struct with device buffers for an M x N tensor (K = N);
+ *            N % 16 == 0.
+ */
+nvfp4_status nvfp4_gemm_quantize(const nvfp4_tensor* A, const nvfp4_tensor* B, const float* amax_in, void* D,
+                                 int64_t ldd, float* amax_out, nvfp4_tensor* out, void* stream);
+
+/*
  * nvfp4_gemm_grouped - `count` independent GEMMs D[e] = A[e] * B[e]^T in one
  * launch (routed experts).  A, B: host arrays of `count` tensors; D: host
  * array of `count` device pointers, each row-major [M_e][N_e] (ldd = N_e, so

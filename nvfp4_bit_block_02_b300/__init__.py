@@ -75,12 +75,14 @@ def lib() -> ctypes.CDLL:
                                              ctypes.POINTER(CQuantConfig), ctypes.POINTER(CTensor), P]
         L.nvfp4_gemm.argtypes = [ctypes.POINTER(CTensor), ctypes.POINTER(CTensor), P, ctypes.c_int, I64, P]
         L.nvfp4_gemm_amax.argtypes = [ctypes.POINTER(CTensor), ctypes.POINTER(CTensor), P, ctypes.c_int, I64, P, P]
+        L.nvfp4_gemm_quantize.argtypes = [ctypes.POINTER(CTensor), ctypes.POINTER(CTensor), P, P, I64, P,
+                                          ctypes.POINTER(CTensor), P]
         L.nvfp4_gemm_grouped.argtypes = [ctypes.c_int, ctypes.POINTER(CTensor), ctypes.POINTER(CTensor),
                                          ctypes.POINTER(ctypes.c_void_p), ctypes.c_int, P]
         L.nvfp4_w4a16_gemm.argtypes = [P, ctypes.c_int, I64, I64, ctypes.POINTER(CTensor), P, ctypes.c_int, I64, P]
         L.nvfp4_sync_check.argtypes = [P]
         for fn in ("nvfp4_amax", "nvfp4_quantize", "nvfp4_quantize_grouped", "nvfp4_rht_quantize", "nvfp4_dequantize",
-                   "nvfp4_transpose_2d", "nvfp4_gemm", "nvfp4_gemm_amax", "nvfp4_gemm_grouped", "nvfp4_w4a16_gemm",
+                   "nvfp4_transpose_2d", "nvfp4_gemm", "nvfp4_gemm_amax", "nvfp4_gemm_quantize", "nvfp4_gemm_grouped", "nvfp4_w4a16_gemm",
                    "nvfp4_sync_check"):
             getattr(L, fn).restype = ctypes.c_int
         L.nvfp4_status_string.argtypes = [ctypes.c_int]
@@ -270,6 +272,23 @@ def gemm_amax(a: NVFP4Tensor, b: NVFP4Tensor, out_dtype=torch.bfloat16, out: tor
     _check(lib().nvfp4_gemm_amax(ctypes.byref(ca), ctypes.byref(cb), _ptr(out), _dtype_code(out.dtype), out.stride(0),
                                  _ptr(amax_out), _stream(stream)), "nvfp4_gemm_amax")
     return out, amax_out
+
+
+def gemm_quantize(a: NVFP4Tensor, b: NVFP4Tensor, amax_in: torch.Tensor, out: NVFP4Tensor | None = None,
+                  d: torch.Tensor | None = None, amax_out: torch.Tensor | None = None, stream=None) -> NVFP4Tensor:
+    """nvfp4_gemm_quantize: D = A * B^T rounded to BF16 and encoded in the GEMM
+    epilogue as the M x N NVFP4 tensor ``out`` (1D blocks along N, RNE,
+    max-6, tensor amax ``amax_in``).  ``d`` (BF16 [M, N] view, optional)
+    also receives D; ``amax_out`` (optional) receives max |D|."""
+    if out is None:
+        out = NVFP4Tensor.empty(a.rows, b.rows, device=a.codes.device)
+    if d is not None and (d.dtype != torch.bfloat16 or d.stride(1) != 1):
+        raise ValueError("d must be BF16 with unit column stride")
+    ca, cb, co = a.c(), b.c(), out.c()
+    _check(lib().nvfp4_gemm_quantize(ctypes.byref(ca), ctypes.byref(cb), _ptr(amax_in), _ptr(d),
+                                     d.stride(0) if d is not None else b.rows, _ptr(amax_out), ctypes.byref(co),
+                                     _stream(stream)), "nvfp4_gemm_quantize")
+    return out
 
 
 def gemm_grouped(a: list, b: list, out_dtype=torch.bfloat16, out: list | None = None, stream=None) -> list:

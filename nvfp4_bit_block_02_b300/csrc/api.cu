@@ -339,6 +339,40 @@ nvfp4_status nvfp4_gemm_amax(const nvfp4_tensor* A, const nvfp4_tensor* B, void*
   return run_gemm(A, B, D, dt, ldd, amax_out, stream);
 }
 
+nvfp4_status nvfp4_gemm_quantize(const nvfp4_tensor* A, const nvfp4_tensor* B, const float* amax_in, void* D,
+                                 int64_t ldd, float* amax_out, nvfp4_tensor* out, void* stream) {
+  nvfp4_status st = check_gemm_operands(A, B);
+  if (st != NVFP4_OK) return st;
+  if (!amax_in) return fail(NVFP4_ERR_INVALID_ARG, "amax_in is NULL");
+  st = check_tensor_buffers(out, "out");
+  if (st != NVFP4_OK) return st;
+  const int64_t M = A->rows, N = B->rows;
+  if (out->rows != M || out->cols != N)
+    return fail(NVFP4_ERR_INVALID_ARG, "out must be M x N (" + std::to_string(M) + " x " + std::to_string(N) + ")");
+  if (N % 16) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "N (the encoded tensor's K) must be a multiple of 16");
+  if (A->cols == 0) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "K must be positive");
+  if (amax_out && (amax_out == amax_in || amax_out == out->amax))
+    return fail(NVFP4_ERR_INVALID_ARG, "amax_out must not alias amax_in or out->amax");
+  if (D) {
+    if (ldd < N) return fail(NVFP4_ERR_INVALID_ARG, "ldd < N");
+    if (!aligned16(D) || (ldd * 2) % 16) return fail(NVFP4_ERR_MISALIGNED, "D must be 16-byte aligned, ldd % 8 == 0");
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (amax_out) {
+    cudaError_t e = cudaMemsetAsync(amax_out, 0, sizeof(float), s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(amax_out)");
+  }
+  if (M == 0 || N == 0) {
+    cudaError_t e = nvfp4::launch_empty_scalars(out->amax, out->global_scale, s);
+    return e == cudaSuccess ? NVFP4_OK : cuda_fail(e, "empty-tensor scalars");
+  }
+  nvfp4::GemmQuantOut q{out->codes, out->scales, out->global_scale, out->amax, amax_in, D ? 1 : 0};
+  const char* why = "";
+  cudaError_t e = nvfp4::launch_gemm(operand(A), operand(B), D, D ? ldd : N, true, s, &why, amax_out, &q);
+  if (e != cudaSuccess) return cuda_fail(e, (std::string("gemm launch: ") + why).c_str());
+  return NVFP4_OK;
+}
+
 nvfp4_status nvfp4_gemm_grouped(int count, const nvfp4_tensor* A, const nvfp4_tensor* B, void* const* D,
                                 nvfp4_dtype dt, void* stream) {
   if (count < 0 || count > NVFP4_MAX_GROUPS) return fail(NVFP4_ERR_INVALID_ARG, "count out of range");

@@ -44,6 +44,7 @@
 #include <cstdint>
 
 #include "gemm.h"
+#include "nvfp4_device.cuh"
 
 namespace nvfp4 {
 namespace {
@@ -327,9 +328,49 @@ struct GroupedSched {
   }
 };
 
-template <class Sched>
+// Encode one epilogue thread's row segment of BF16 outputs (128 columns from
+// col0, packed two per word) as NVFP4 with 1D blocks along N: exactly the
+// encoder's max-6 / round-to-nearest-even sequence (include/nvfp4.h) with g
+// from the supplied amax.  Codes go to row r of the [M][N/2] code matrix; the
+// two 4-block scale words to their atoms (zeros for rows >= M and blocks past
+// N, which are the layout's padding).
+__device__ __forceinline__ void encode_row_segment(const GemmQuantOut& qo, const uint32_t (&pk)[64], int r, int col0,
+                                                   int M, int N, float g, float g6) {
+  const int KB = N >> 4, nka = (KB + 3) >> 2;
+  const bool row_ok = r < M;
+  uint32_t sw[2] = {0u, 0u};
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int kb = (col0 >> 4) + j;
+    if (row_ok && kb < KB) {
+      float v[16];
+      uint32_t mx = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t w = pk[8 * j + i];
+        v[2 * i] = bf16_lo(w);
+        v[2 * i + 1] = bf16_hi(w);
+        mx = __vmaxu2(mx, w & 0x7FFF7FFFu);
+      }
+      const float amax_b = __uint_as_float(max(mx & 0xFFFFu, mx >> 16) << 16);
+      float sv, rcp;
+      const uint32_t sb = block_scale(amax_b, g6, g, sv, rcp);
+      *reinterpret_cast<uint2*>(qo.codes + (int64_t)r * (N >> 1) + kb * 8) = encode16<false>(v, rcp, nullptr);
+      sw[j >> 2] |= sb << (8 * (j & 3));
+    }
+  }
+#pragma unroll
+  for (int a = 0; a < 2; ++a) {
+    const int ka = (col0 >> 6) + a;
+    if (ka < nka)
+      *reinterpret_cast<uint32_t*>(qo.scales + ((int64_t)(r >> 7) * nka + ka) * 512 + (r & 31) * 16 +
+                                   ((r >> 5) & 3) * 4) = sw[a];
+  }
+}
+
+template <class Sched, bool QOUT = false>
 __device__ __forceinline__ void gemm_pairs(const Sched& sched, bool out_bf16, unsigned int* err,
-                                           unsigned int* amax_out) {
+                                           unsigned int* amax_out, const GemmQuantOut* qo = nullptr) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
@@ -347,6 +388,13 @@ __device__ __forceinline__ void gemm_pairs(const Sched& sched, bool out_bf16, un
   const int num_tiles = sched.num_tiles();
   const int first = (int)cluster_id(), step = (int)num_clusters();
 
+  if constexpr (QOUT) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) {  // the encoded tensor's scalars
+      const float amax = *qo->amax_in;
+      *qo->global_scale = global_scale(amax);
+      *qo->amax = amax;
+    }
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full0 + 8 * s, 1 + 8);
@@ -592,7 +640,15 @@ __device__ __forceinline__ void gemm_pairs(const Sched& sched, bool out_bf16, un
           m = __reduce_max_sync(0xFFFFFFFFu, m);
           if (lane == 0 && m) atomicMax(amax_out, m);
         }
-        if (active) {
+        if constexpr (QOUT) {
+          // the next layer's NVFP4 input from the BF16 values just formed; a
+          // CTA whose 128 rows start below M owns its scale atoms' padding too
+          if ((2 * x.pm + (int)rank) * BM < x.M && col0 < x.N) {
+            const float g = global_scale(*qo->amax_in);
+            encode_row_segment(*qo, pk, row0 + lane, col0, x.M, x.N, g, __fmul_rn(6.0f, g));
+          }
+        }
+        if (active && (!QOUT || qo->store_d)) {
 #pragma unroll
           for (int cc = 0; cc < 2; ++cc) {  // 64 columns = one 128-byte box row
             if (64 * cc >= ncols) break;
@@ -673,6 +729,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   gemm_pairs(s, a.out_bf16 != 0, a.err, a.amax_out);
 }
 
+// The GEMM with the NVFP4 encoding of its BF16 output in the epilogue.
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    k_gemm_quant(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                 const __grid_constant__ CUtensorMap tmD, const __grid_constant__ GemmArgs a) {
+  SingleSched s{&tmA, &tmB, &tmD, &a};
+  gemm_pairs<SingleSched, true>(s, true, a.err, a.amax_out, &a.q);
+}
+
 __global__ void __launch_bounds__(NUM_THREADS, 1) k_gemm_grouped(const __grid_constant__ GroupedArgs g) {
   GroupedSched s{&g};
   gemm_pairs(s, g.out_bf16 != 0, g.err, nullptr);
@@ -742,7 +806,7 @@ bool make_out_map(CUtensorMap* m, void* d, int64_t rows, int64_t cols, int64_t l
 // concurrent first calls compute the same values, and the atomics make the
 // publication safe.
 constexpr int kMaxDevices = 64;
-enum KernelId { kSingle = 0, kGrouped = 1, kNumKernels = 2 };
+enum KernelId { kSingle = 0, kGrouped = 1, kSingleQuant = 2, kNumKernels = 3 };
 struct DeviceState {
   std::atomic<unsigned int*> err{nullptr};
   std::atomic<unsigned int*> err_taken{nullptr};
@@ -844,10 +908,10 @@ int gemm_tile_m() { return 2 * BM; }
 int gemm_tile_n() { return BN; }
 
 cudaError_t launch_gemm(const GemmOperand& A, const GemmOperand& B, void* D, int64_t ldd, bool out_bf16, cudaStream_t s,
-                        const char** why, float* amax_out) {
-  CUtensorMap ta, tb, td;
+                        const char** why, float* amax_out, const GemmQuantOut* q) {
+  CUtensorMap ta, tb, td = {};
   if (!make_code_map(&ta, A.codes, A.rows, A.K) || !make_code_map(&tb, B.codes, B.rows, B.K) ||
-      !make_out_map(&td, D, A.rows, B.rows, ldd, out_bf16)) {
+      (D && !make_out_map(&td, D, A.rows, B.rows, ldd, out_bf16))) {
     *why = "cuTensorMapEncodeTiled failed (or driver entry point unavailable)";
     return cudaErrorInvalidValue;
   }
@@ -857,14 +921,16 @@ cudaError_t launch_gemm(const GemmOperand& A, const GemmOperand& B, void* D, int
     *why = "device error word unavailable";
     return cudaErrorInvalidValue;
   }
-  if (!smem_configured(st, kSingle, reinterpret_cast<const void*>(k_gemm))) {
+  const KernelId kid = q ? kSingleQuant : kSingle;
+  auto kernel = q ? k_gemm_quant : k_gemm;
+  if (!smem_configured(st, kid, reinterpret_cast<const void*>(kernel))) {
     *why = "cudaFuncSetAttribute failed";
     return cudaErrorInvalidValue;
   }
   GemmArgs a{A.scales, B.scales, A.g, B.g, (int)A.rows, (int)B.rows, (int)A.K, out_bf16 ? 1 : 0, err,
-             reinterpret_cast<unsigned int*>(amax_out)};
+             reinterpret_cast<unsigned int*>(amax_out), q ? *q : GemmQuantOut{}};
   const int tiles = (int)((A.rows + 2 * BM - 1) / (2 * BM)) * (int)((B.rows + BN - 1) / BN);
-  cudaError_t e = launch_pairs(k_gemm, tiles, st, kSingle, s, ta, tb, td, a);
+  cudaError_t e = launch_pairs(kernel, tiles, st, kid, s, ta, tb, td, a);
   if (e != cudaSuccess) *why = "cudaLaunchKernelEx (cluster of 2) failed";
   return e;
 }

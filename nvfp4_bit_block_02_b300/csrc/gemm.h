@@ -14,6 +14,18 @@ struct GemmOperand {
   int64_t rows, K;
 };
 
+// The epilogue's NVFP4 encoding of the BF16-rounded output (the next layer's
+// input): 1D blocks of 16 along N, round to nearest even, max-6, with the
+// tensor amax supplied.
+struct GemmQuantOut {
+  uint8_t* codes;         // [M][N/2]
+  uint8_t* scales;        // 128 x 4-block atoms, ceil(M/128)*128 x ceil(N/64)*4 bytes
+  float* global_scale;    // written: g = fl(amax / 2688) (1 if amax = 0)
+  float* amax;            // written: the amax used
+  const float* amax_in;   // read: the tensor amax to encode with
+  int store_d;            // 0: D itself is not written
+};
+
 struct GemmArgs {
   const uint8_t* sfa;
   const uint8_t* sfb;
@@ -23,6 +35,7 @@ struct GemmArgs {
   int out_bf16;
   unsigned int* err;
   unsigned int* amax_out;  // nullable: atomicMax of |D| (as stored) over the output, float bits
+  GemmQuantOut q;          // used by the quantizing variant only
 };
 
 constexpr int kGroupsPerLaunch = 64;
@@ -49,7 +62,7 @@ cudaError_t take_device_error(cudaStream_t s, unsigned int* value);
 int gemm_tile_m();
 int gemm_tile_n();
 cudaError_t launch_gemm(const GemmOperand& A, const GemmOperand& B, void* D, int64_t ldd, bool out_bf16, cudaStream_t s,
-                        const char** why, float* amax_out = nullptr);
+                        const char** why, float* amax_out = nullptr, const GemmQuantOut* q = nullptr);
 cudaError_t launch_gemm_grouped(int count, const GemmOperand* A, const GemmOperand* B, void* const* D, bool out_bf16,
                                 cudaStream_t s, const char** why);
 

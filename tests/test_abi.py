@@ -29,7 +29,7 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for required in ["nvfp4_amax", "nvfp4_quantize", "nvfp4_quantize_grouped", "nvfp4_rht_quantize", "nvfp4_dequantize",
-                     "nvfp4_transpose_2d", "nvfp4_gemm", "nvfp4_gemm_amax",
+                     "nvfp4_transpose_2d", "nvfp4_gemm", "nvfp4_gemm_amax", "nvfp4_gemm_quantize",
                      "nvfp4_gemm_grouped", "nvfp4_w4a16_gemm", "nvfp4_codes_bytes", "nvfp4_scales_bytes", "nvfp4_sync_check",
                      "nvfp4_status_string", "nvfp4_last_error"]:
         assert required in names
@@ -193,3 +193,22 @@ def test_w4a16_argument_errors(L):
     big = (1 << 28) + 16                                                                  # K beyond the kernel's offsets
     assert call(x, nv.BF16, 1, big, ctypes.byref(_fake_tensor(16, big)), y, nv.BF16, 16, None) == 2
     assert "too large" in L.nvfp4_last_error().decode()
+
+
+def test_gemm_quantize_argument_errors(L):
+    A = _fake_tensor(128, 256)
+    B = _fake_tensor(256, 256, base=0x800000)
+    out = _fake_tensor(128, 256, base=0xC00000)
+    amax = ctypes.c_void_p(0x5000000)
+    D = ctypes.c_void_p(0x4000000)
+    call = L.nvfp4_gemm_quantize
+    assert call(ctypes.byref(A), ctypes.byref(B), None, D, 256, None, ctypes.byref(out), None) == 1   # amax_in NULL
+    assert call(ctypes.byref(A), ctypes.byref(B), amax, D, 256, None, None, None) == 1                # out NULL
+    bad = _fake_tensor(128, 128, base=0xC00000)
+    assert call(ctypes.byref(A), ctypes.byref(B), amax, D, 256, None, ctypes.byref(bad), None) == 1   # out not M x N
+    B2, o2 = _fake_tensor(264, 256, base=0x800000), _fake_tensor(128, 264, base=0xC00000)
+    assert call(ctypes.byref(A), ctypes.byref(B2), amax, None, 0, None, ctypes.byref(o2), None) == 2  # N % 16
+    assert call(ctypes.byref(A), ctypes.byref(B), amax, D, 200, None, ctypes.byref(out), None) == 1   # ldd < N
+    assert call(ctypes.byref(A), ctypes.byref(B), amax, ctypes.c_void_p(0x4000008), 256, None, ctypes.byref(out),
+                None) == 3                                                                          # D misaligned
+    assert call(ctypes.byref(A), ctypes.byref(B), amax, D, 256, amax, ctypes.byref(out), None) == 1   # aliasing
