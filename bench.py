@@ -263,6 +263,48 @@ def encode_rates(nv, x, w, dev, reps=24):
     return out
 
 
+def next_input_rates(nv, qa, qb, d, dev, flush, reps=10):
+    """GEMM -> the next layer's NVFP4 input (its BF16 output quantized 1D,
+    RNE, max-6 with the producer amax), three ways, each a CUDA graph timed
+    between events with an L2 flush before every replay: the GEMM with the
+    producer amax then the quantizer over D; the GEMM with the encoding in
+    its epilogue and D not stored; the same with D stored."""
+    M, N = qa.rows, qb.rows
+    amax = torch.zeros(1, dtype=torch.float32, device=dev)
+    amax_next = torch.zeros(1, dtype=torch.float32, device=dev)
+    nv.gemm_amax(qa, qb, out=d, amax_out=amax)
+    qd = nv.NVFP4Tensor.empty(M, N, device=dev)
+    variants = {
+        "gemm_amax_then_quantize": lambda: (nv.gemm_amax(qa, qb, out=d, amax_out=amax_next),
+                                            nv.quantize(d, amax=amax_next, out=qd)),
+        "gemm_quantize_fused": lambda: nv.gemm_quantize(qa, qb, amax, out=qd),
+        "gemm_quantize_fused_with_d": lambda: nv.gemm_quantize(qa, qb, amax, out=qd, d=d),
+    }
+    out = {}
+    side = torch.cuda.Stream(dev)
+    for name, fn in variants.items():
+        side.wait_stream(torch.cuda.current_stream(dev))
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            fn()
+            with torch.cuda.graph(g, stream=side):
+                fn()
+        torch.cuda.current_stream(dev).wait_stream(side)
+        ts = []
+        for _ in range(reps + 2):
+            flush.zero_()
+            st, en = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            st.record()
+            g.replay()
+            en.record()
+            torch.cuda.synchronize(dev)
+            ts.append(st.elapsed_time(en))
+        out[name] = {"us": round(statistics.median(ts[2:]) * 1e3, 2)}
+        del g
+    nv.sync_check()
+    return out
+
+
 # --------------------------------------------------------------------------
 # our implementation
 # --------------------------------------------------------------------------
@@ -300,7 +342,8 @@ def make_plan(workload: str, nv, synthetic, dev):
                  ("quantize_W_2d", lambda: nv.quantize(b, block="2d", out=qb), b.numel(), es)]
     parts.append(("gemm", lambda: nv.gemm(qa, qb, out=d), None, None))
     # RHT: an amax-only pass of the transform and the encode; plain: amax + encode; GEMM: 1
-    return dict(inputs_h=[a_h, b_h], inputs=[a, b], parts=parts, out=d, M=M, N=N, K=K, launches=5, fwd=(a, b))
+    return dict(inputs_h=[a_h, b_h], inputs=[a, b], parts=parts, out=d, M=M, N=N, K=K, launches=5, fwd=(a, b),
+                q=(qa, qb))
 
 
 def run_ours(args, rank, world, local_rank):
@@ -385,6 +428,7 @@ def run_ours(args, rank, world, local_rank):
     t_parts = [[evc[i][j].elapsed_time(evc[i][j + 1]) for i in range(args.steps)] for j in range(3)]
     t_gm = t_parts[2]
     enc = encode_rates(nv, x, w, dev) if rank == 0 and args.workload in ("llama8b", "llama405b") else None
+    nxt = next_input_rates(nv, *plan["q"], d, dev, flush) if rank == 0 and args.workload in ("llama8b",) else None
     # end to end through the public API from pinned host buffers, D read back.
     # Every step uploads its X and W and reads back all of D.  The read-back
     # runs on a stream of its own (the opposite direction of the host link),
@@ -472,6 +516,8 @@ def run_ours(args, rank, world, local_rank):
             **comps,
             "gemm": {"ms": round(gemm_ms, 4), "TFLOP_s": round(gemm_tflops, 1),
                      "frac_of_fp4_peak": round(gemm_tflops / fp4_peak, 4)},
+            # GEMM -> next layer's NVFP4 input (D quantized with the producer amax): unfused vs fused epilogue
+            "next_layer_input": nxt,
             # the encode kernel alone (tensor amax supplied), the quantizer's roofline figure
             "roofline_quantize": ({"bound": "hbm", "kernel": "k_quant_rows (X 1D RNE)",
                                    "achieved": enc_line["X"]["GB_s"], "peak": hbm, "unit": "GB/s",
@@ -845,12 +891,12 @@ def _linear_fit(n1: int, t1: float, n2: int, t2: float):
     return max(t1 - b * n1, 0.0), b
 
 
-# Per workload, the slices the oracle is timed on: (X rows, W rows, GEMM output rows), each part timed at that
-# size and at twice it.  Fprop: rows of X (1D) and of W (2D); the GEMM reference runs those output rows against
-# the W slice.  Wgrad: columns of dY and of X (transposed RHT quantization).  The 1-core figure uses the
-# sizes divided by _ONE_CORE_DIV.
-_ORACLE_SLICES = {"llama8b": (2048, 3584, 512), "llama405b": (512, 1024, 256), "wgrad": (1024, 512, 512),
-                  "pr1": (128, 128, 128)}
+# Per workload, the slices the oracle is timed on: (X rows, W rows, GEMM output rows, GEMM output columns).  The
+# quantizations are timed at n and 2n rows (fprop: rows of X 1D and W 2D; Wgrad: columns of dY and X, transposed RHT);
+# the fp64 GEMM reference on a 2 x 2 grid of (rows, columns) = (g or 2g, c or 2c) cut from those operands.  The 1-core
+# figure divides every size by _ONE_CORE_DIV.
+_ORACLE_SLICES = {"llama8b": (2048, 3584, 1024, 1024), "llama405b": (512, 1024, 256, 512),
+                  "wgrad": (1024, 512, 512, 512), "pr1": (128, 128, 128, 128)}
 _ONE_CORE_DIV = 8
 
 
@@ -888,7 +934,7 @@ def _oracle_step(workload: str, X, W, div: int = 1) -> dict:
         return {"step_s": c["E"] * t, "spent_s": t,
                 "parts": {"quantize_w_s": round(tw, 4), "quantize_x_s": round(tx, 4), "gemm_s": round(tg, 4)},
                 "work": f"one whole expert (W_e^T Four-over-Six, X_e, GEMM {c['M']}x{N}x{c['K']}), x{c['E']}"}
-    rx, rw, rg = (max(1, v // div) for v in _ORACLE_SLICES[workload])
+    rx, rw, rg, rc = (max(1, v // div) for v in _ORACLE_SLICES[workload])
     if workload == "pr1":   # the whole step is small: time it as it is
         tq1, qa = _time(lambda: oracle.quantize(X))
         tq2, qb = _time(lambda: oracle.quantize(W))
@@ -903,24 +949,34 @@ def _oracle_step(workload: str, X, W, div: int = 1) -> dict:
     else:
         qa_fn = lambda n: oracle.quantize(X[:n])
         qb_fn = lambda n: oracle.quantize(W[:n], block2d=True)
-    spent = 0.0
-    fits = {}
     ta1, _ = _time(lambda: qa_fn(rx))
     ta2, qa = _time(lambda: qa_fn(2 * rx))
     tb1, _ = _time(lambda: qb_fn(rw))
     tb2, qb = _time(lambda: qb_fn(2 * rw))
-    tg1, _ = _time(lambda: oracle.gemm_reference(qa, qb, rows=np.arange(rg)))
-    tg2, _ = _time(lambda: oracle.gemm_reference(qa, qb, rows=np.arange(2 * rg)))
-    spent = ta1 + ta2 + tb1 + tb2 + tg1 + tg2
-    fa, fb, fg = _linear_fit(rx, ta1, 2 * rx, ta2), _linear_fit(rw, tb1, 2 * rw, tb2), _linear_fit(rg, tg1, 2 * rg, tg2)
-    step = (fa[0] + fa[1] * M) + (fb[0] + fb[1] * N) + (fg[0] + fg[1] * M) * (N / (2 * rw))
-    for name, (a, b), n, t in (("quantize_a", fa, rx, ta1), ("quantize_b", fb, rw, tb1), ("gemm", fg, rg, tg1)):
-        fits[name] = {"fixed_s": round(a, 5), "per_unit_us": round(b * 1e6, 4), "fixed_frac_at_n": round(a / t, 4)}
+    fa, fb = _linear_fit(rx, ta1, 2 * rx, ta2), _linear_fit(rw, tb1, 2 * rw, tb2)
+    # GEMM reference: t(g, c) = c0 + cA*g + cB*c + cAB*g*c (operand conversions and the products), from the
+    # 2 x 2 grid of output rows g and output columns c
+    cols = lambda c: oracle.Quantized(qb.codes[:c], qb.scales[:c], qb.amax, qb.g, None, None, c, qb.K)
+    tg = {(g, c): _time(lambda: oracle.gemm_reference(qa, cols(c), rows=np.arange(g)))[0]
+          for g in (rg, 2 * rg) for c in (rc, 2 * rc)}
+    t11, t21, t12, t22 = tg[rg, rc], tg[2 * rg, rc], tg[rg, 2 * rc], tg[2 * rg, 2 * rc]
+    cab = max((t22 - t21 - t12 + t11) / (rg * rc), 0.0)
+    ca = max((t21 - t11) / rg - cab * rc, 0.0)
+    cb = max((t12 - t11) / rc - cab * rg, 0.0)
+    c0 = max(t11 - ca * rg - cb * rc - cab * rg * rc, 0.0)
+    t_gemm = c0 + ca * M + cb * N + cab * M * N
+    step = (fa[0] + fa[1] * M) + (fb[0] + fb[1] * N) + t_gemm
+    spent = ta1 + ta2 + tb1 + tb2 + sum(tg.values())
+    parts = {name: {"fixed_s": round(a, 5), "per_unit_us": round(b * 1e6, 4), "fixed_frac_at_n": round(a / t, 4)}
+             for name, (a, b), t in (("quantize_a", fa, ta1), ("quantize_b", fb, tb1))}
+    parts["gemm"] = {"fixed_s": round(c0, 5), "per_row_us": round(ca * 1e6, 3), "per_col_us": round(cb * 1e6, 3),
+                     "per_output_ns": round(cab * 1e9, 3), "whole_step_s": round(t_gemm, 3),
+                     "products_frac_at_sample": round(cab * 4 * rg * rc / t22, 4)}
     unit = "columns" if workload == "wgrad" else "rows"
-    return {"step_s": step, "spent_s": spent, "parts": fits,
-            "work": (f"quantize A {unit} [0,{rx}) and [0,{2 * rx}), B {unit} [0,{rw}) and [0,{2 * rw}), fp64 GEMM of "
-                     f"{rg} and {2 * rg} output rows x {2 * rw} columns; each part fit as a + b*n and extrapolated "
-                     f"to the whole step")}
+    return {"step_s": step, "spent_s": spent, "parts": parts,
+            "work": (f"quantize A {unit} [0,{rx}) and [0,{2 * rx}), B {unit} [0,{rw}) and [0,{2 * rw}) (each fit as "
+                     f"a + b*n); fp64 GEMM reference on output blocks of {rg} or {2 * rg} rows x {rc} or {2 * rc} "
+                     f"columns (fit as c0 + cA*rows + cB*cols + cAB*rows*cols); extrapolated to the whole step")}
 
 
 def _set_threads(n: int | None):

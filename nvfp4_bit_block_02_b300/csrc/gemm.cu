@@ -484,11 +484,19 @@ __device__ __forceinline__ void gemm_pairs(const Sched& sched, bool out_bf16, un
           const uint32_t sn = s + 1 == STAGES ? 0 : s + 1, phn = s + 1 == STAGES ? ph ^ 1 : ph;
           const uint64_t da = da0 + (uint64_t)(s * (A_BYTES >> 4)), db = db0 + (uint64_t)(s * (B_BYTES >> 4));
           const uint32_t sfa = tmem + SFA_COL0 + 16 * s, sfb = tmem + SFB_COL0 + 32 * s;
-          const int kc = min(4, nkc - 4 * kt);  // K-steps of 64 in this stage (4 except at a K tail)
+          const int kc = nkc - 4 * kt;  // K-steps of 64 left: 4 or more except in a K-tail stage
+          if (kc >= 4) {
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            if (j < kc) tc_mma_pair(tmem, da + 2 * j, db + 2 * j, sfa + 4 * j, sfb + 8 * j, (kt | j) != 0);
-            if (j == 2) next_ready = mbar_test(full0 + 8 * sn, phn);
+            for (int j = 0; j < 4; ++j) {
+              tc_mma_pair(tmem, da + 2 * j, db + 2 * j, sfa + 4 * j, sfb + 8 * j, (kt | j) != 0);
+              if (j == 2) next_ready = mbar_test(full0 + 8 * sn, phn);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              if (j < kc) tc_mma_pair(tmem, da + 2 * j, db + 2 * j, sfa + 4 * j, sfb + 8 * j, (kt | j) != 0);
+              if (j == 2) next_ready = mbar_test(full0 + 8 * sn, phn);
+            }
           }
           tc_commit_pair(empty0 + 8 * s);
           s = sn;
