@@ -61,27 +61,23 @@ __device__ __forceinline__ float e2m1_value(uint32_t code) {
   return (code & 8u) ? -v : v;
 }
 
-// Stochastic rounding of q to a 4-bit code with a 16-bit uniform number:
-// neighbours lo <= |q| < hi on the grid, frac = (|q| - lo) / (hi - lo),
-// round up iff u16 < fl(frac * 65536); |q| >= 6 saturates.  The grid step of
-// |q|'s binade is 0.5, 1 or 2, so with t = |q| / step (exact), lo = floor(t)
-// steps and frac * 65536 = T - 65536 * floor(t), T = t * 65536 (exact).  For an
-// integer u16, u16 < frac * 65536 iff ceil(T) + 65535 - u16 reaches the next
-// multiple of 65536, so the code index is (ceil(T) + (u16 ^ 0xFFFF)) >> 16 plus
-// the binade's first index.  ceil(T) comes from one fma rounded upward onto
-// the integer grid of [2^23, 2^24): every step is exact integer or IEEE
-// arithmetic, no conversion or floor instruction is needed, and |q| >= 6
-// (and any larger value, up to infinity) lands on index 7 through the min.
-__device__ __forceinline__ uint32_t e2m1_sr(float q, uint32_t u16) {
-  const uint32_t sign = (__float_as_uint(q) >> 28) & 8u;
-  const float a = fabsf(q);
-  const bool lt2 = a < 2.0f, lt4 = a < 4.0f;
-  const float k = lt2 ? 131072.0f : (lt4 ? 65536.0f : 32768.0f);  // 65536 / step
-  // 2^23's bit pattern is removed and the binade's first index (0, 2, 4) added
-  const uint32_t bias = lt2 ? 0xB5000000u : (lt4 ? 0xB5020000u : 0xB5040000u);
-  const float c = __fmaf_ru(a, k, 8388608.0f);  // 2^23 + ceil(T)
-  const uint32_t idx = (__float_as_uint(c) + (u16 ^ 0xFFFFu) + bias) >> 16;
-  return sign | min(idx, 7u);
+// Stochastic rounding of a = |q| to an E2M1 magnitude index with a 16-bit
+// uniform number u, given as nu = 65535 - u: neighbours lo <= a < hi on the
+// grid, frac = (a - lo) / (hi - lo), round up iff u < fl(frac * 65536);
+// a >= 6 saturates.  Write idx(a) for the grid position of a (0, 0.5, 1, 1.5,
+// 2, 3, 4, 6 sit at 0..7; linear in between), so the result is
+// floor(idx) + [u < frac * 65536] with frac = idx - floor(idx).  For an
+// integer u that is (ceil(T) + 65535 - u) >> 16 with T = 65536 * idx (exact):
+// ceil(T) + nu reaches the next multiple of 65536 iff ceil(frac * 65536) > u.
+// T itself: on [0, 1) the grid is uniform, T = 131072 * a, and ceil(T) comes
+// from one fma rounded upward onto the integer grid of [2^23, 2^24); on
+// [1, 8) every binade holds two grid steps, so T is linear in the float's
+// bit pattern: T = (bits(a) - bits(0.5)) / 64, ceil(T) = (bits(a) - bits(0.5)
+// + 63) >> 6.  Above 6 (and at infinity) the min saturates to index 7.
+__device__ __forceinline__ uint32_t e2m1_sr_index(float a, uint32_t nu) {
+  const uint32_t tl = __float_as_uint(__fmaf_ru(a, 131072.0f, 8388608.0f)) - 0x4B000000u;
+  const uint32_t tg = (__float_as_uint(a) - 0x3F000000u + 63u) >> 6;
+  return min(((a < 1.0f ? tl : tg) + nu) >> 16, 7u);
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -105,18 +101,21 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
 
 // The 16 rounding draws of the 16 elements starting at output-orientation
 // linear index i0 (i0 % 16 == 0): element e draws half (e & 1) of word
-// (e % 8) / 2 of the call with counter i0 / 8 + e / 8.
-__device__ __forceinline__ void sr_draws16(uint64_t seed, uint64_t offset, uint64_t i0, uint32_t u[16]) {
+// (e % 8) / 2 of the call with counter i0 / 8 + e / 8.  Returned
+// complemented, nu[e] = 65535 - u[e], the form e2m1_sr_index takes.
+__device__ __forceinline__ void sr_draws16(uint64_t seed, uint64_t offset, uint64_t i0, uint32_t nu[16]) {
   uint64_t j = i0 >> 3;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     uint64_t jj = j + h;
     uint4 w = philox4x32_10(make_uint4((uint32_t)jj, (uint32_t)(jj >> 32), (uint32_t)offset, (uint32_t)(offset >> 32)),
                             (uint32_t)seed, (uint32_t)(seed >> 32));
-    u[8 * h + 0] = w.x & 0xFFFFu; u[8 * h + 1] = w.x >> 16;
-    u[8 * h + 2] = w.y & 0xFFFFu; u[8 * h + 3] = w.y >> 16;
-    u[8 * h + 4] = w.z & 0xFFFFu; u[8 * h + 5] = w.z >> 16;
-    u[8 * h + 6] = w.w & 0xFFFFu; u[8 * h + 7] = w.w >> 16;
+    const uint32_t c[4] = {~w.x, ~w.y, ~w.z, ~w.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      nu[8 * h + 2 * k] = c[k] & 0xFFFFu;
+      nu[8 * h + 2 * k + 1] = c[k] >> 16;
+    }
   }
 }
 
@@ -251,7 +250,8 @@ __device__ __forceinline__ uint32_t block_scale(float amax_b, float mg, float g,
   return b;
 }
 
-// Encode 16 values with block reciprocal rcp into two 32-bit words of codes.
+// Encode 16 values with block reciprocal rcp into two 32-bit words of codes
+// (u: the complemented draws of sr_draws16, used only with SR).
 // The products are paired into packed fp32x2 multiplies (each lane an IEEE
 // round-to-nearest product, the same value as a scalar multiply).
 template <bool SR>
@@ -264,14 +264,17 @@ __device__ __forceinline__ uint2 encode16(const float v[16], float rcp, const ui
     q[2 * i] = p.x;
     q[2 * i + 1] = p.y;
   }
+  const uint2 rne = make_uint2(e2m1x8_rne(q), e2m1x8_rne(q + 8));
   if constexpr (!SR) {
-    return make_uint2(e2m1x8_rne(q), e2m1x8_rne(q + 8));
+    return rne;
   } else {
-    uint32_t w0 = 0, w1 = 0;
+    // magnitudes from stochastic rounding; each code's sign bit is q's sign,
+    // which the round-to-nearest codes already carry (bit 3 of every nibble)
+    uint32_t w0 = rne.x & 0x88888888u, w1 = rne.y & 0x88888888u;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) w0 |= e2m1_sr(q[i], u[i]) << (4 * i);
+    for (int i = 0; i < 8; ++i) w0 += e2m1_sr_index(fabsf(q[i]), u[i]) << (4 * i);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) w1 |= e2m1_sr(q[8 + i], u[8 + i]) << (4 * i);
+    for (int i = 0; i < 8; ++i) w1 += e2m1_sr_index(fabsf(q[8 + i]), u[8 + i]) << (4 * i);
     return make_uint2(w0, w1);
   }
 }
