@@ -102,6 +102,8 @@ nvfp4_status run_quantize(const void* x, nvfp4_dtype xt, int64_t rows, int64_t c
   a.seed = cfg->seed;
   a.offset = cfg->offset;
   a.rht_seed = rht_seed;
+  a.err = nvfp4::device_error_word();
+  if (!a.err) return cuda_fail(cudaGetLastError(), "device error word (cudaGetSymbolAddress)");
   const bool tr = cfg->transpose != 0, b2d = cfg->block == NVFP4_BLOCK_2D,
              sr = cfg->round == NVFP4_ROUND_STOCHASTIC, f46 = cfg->scaling == NVFP4_SCALE_FOUR_OVER_SIX;
   if (!amax) {

@@ -56,6 +56,12 @@ struct GroupedArgs {
 };
 
 unsigned int* device_error_word();
+// A 2D tiled tensor map over a row-major [rows][ld] BF16/FP32 matrix (first
+// `cols` columns), box = box_cols x box_rows elements, no swizzle; boxes past
+// the edges are zero-filled.  False when the driver entry point is missing
+// or the encoding is rejected.
+bool make_tile_map_2d(CUtensorMap* m, const void* base, bool bf16, int64_t rows, int64_t cols, int64_t ld,
+                      uint32_t box_cols, uint32_t box_rows);
 // Read and clear the current device's timeout word in one atomic exchange
 // (ordered on `s`), then synchronise `s` and return the value read.
 cudaError_t take_device_error(cudaStream_t s, unsigned int* value);

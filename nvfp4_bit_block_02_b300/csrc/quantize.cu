@@ -13,6 +13,9 @@
 // encoder and no memset is needed.  Loads are 16-byte vectors; the transposed
 // encoder stages a 64 x 128 input tile in shared memory and reads it back as
 // column pairs (32-bit words), conflict-free.
+#include <atomic>
+
+#include "gemm.h"
 #include "nvfp4_device.cuh"
 #include "quantize.h"
 
@@ -431,12 +434,61 @@ struct ColTile<float> {
   }
 };
 
-template <typename T, bool B2D, bool SR, bool F46, bool RHT, bool AMAX_ONLY, class Src>
-__device__ __forceinline__ void quant_cols_body(const Src& src, const QuantArgs& a0) {
+// TMA ring of the single-tensor transposed encoder: 64 x 128-element input
+// tiles (16 KB in BF16, 32 KB in FP32), 64 KB per CTA, so that the bytes in
+// flight do not depend on the registers the encode needs.
+template <typename T>
+constexpr int kColStages = 65536 / (64 * ColTile<T>::kRowBytes);
+template <typename T>
+constexpr int kColRingBytes = kColStages<T> * 64 * ColTile<T>::kRowBytes;
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ void bar_init(uint64_t* b, uint32_t n) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(b)), "r"(n));
+}
+__device__ __forceinline__ bool bar_test(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait (2 s of global time): false on timeout.
+__device__ __forceinline__ bool bar_wait(uint64_t* b, uint32_t parity) {
+  if (bar_test(b, parity)) return true;
+  unsigned long long t0, t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+  for (uint32_t it = 1;; ++it) {
+    if (bar_test(b, parity)) return true;
+    if ((it & 63u) == 0) {
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+      if (t - t0 > 2000000000ull) return false;
+    }
+  }
+}
+// One 2D tile of x into shared memory, completion counted on `b`.
+__device__ __forceinline__ void tile_load(void* dst, const CUtensorMap* tm, int x, int y, uint64_t* b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(b)), "r"(bytes) : "memory");
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(smem_addr(b))
+      : "memory");
+}
+
+// TMA (single tensor, tm != nullptr) or register prefetch (grouped tensors).
+template <typename T, bool B2D, bool SR, bool F46, bool RHT, bool AMAX_ONLY, bool TMA, class Src>
+__device__ __forceinline__ void quant_cols_body(const Src& src, const QuantArgs& a0, const CUtensorMap* tm = nullptr) {
   constexpr int RB = ColTile<T>::kRowBytes;
   constexpr int VPR = RB / 16;                  // 16-byte vectors per tile row
-  constexpr int NV = (64 * VPR) / 256;          // vectors per thread
-  __shared__ __align__(16) uint8_t tile_s[64 * RB];
+  constexpr int NV = TMA ? 1 : (64 * VPR) / 256;  // vectors per thread (register path)
+  constexpr int S = kColStages<T>;
+  __shared__ __align__(16) uint8_t tile_s[TMA ? 16 : 64 * RB];
+  extern __shared__ __align__(128) uint8_t ring[];
+  __shared__ uint64_t full[TMA ? S : 1];
+  __shared__ int abort_s;
   const int t = threadIdx.x;
   const int np = t & 63, kbl = t >> 6;
   uint32_t mask = 0;
@@ -472,20 +524,47 @@ __device__ __forceinline__ void quant_cols_body(const Src& src, const QuantArgs&
   };
 
   uint4 raw[NV];
-  typename Src::Ref ref;
+  typename Src::Ref ref, iref;  // the tile to encode; (TMA) the next tile to request
   bool have = src.first(ref);
-  if (have) load(ref, raw);
-  while (have) {
-    __syncthreads();  // the previous tile's readers are done with tile_s
+  [[maybe_unused]] bool have_i = have;
+  [[maybe_unused]] uint32_t k = 0;    // this CTA's tile counter (TMA ring position)
+  [[maybe_unused]] uint32_t req = 0;  // (thread 0) tiles requested so far
+  if constexpr (TMA) {
+    if (t == 0) {
+      abort_s = 0;
 #pragma unroll
-    for (int i = 0; i < NV; ++i) {
-      int idx = t + 256 * i, row = idx / VPR, cv = idx % VPR;
-      *reinterpret_cast<uint4*>(tile_s + row * RB + cv * 16) = raw[i];
+      for (int i = 0; i < S; ++i) bar_init(&full[i], 1);
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+      iref = ref;
+      for (int i = 0; i < S && have_i; ++i) {
+        tile_load(ring + i * 64 * RB, tm, (int)(iref.tx * 128), (int)(iref.ty * 64), &full[i], 64 * RB);
+        ++req;
+        typename Src::Ref n;
+        have_i = src.next(iref, n);
+        iref = n;
+      }
     }
     __syncthreads();
+  } else {
+    if (have) load(ref, raw);
+  }
+  while (have) {
+    const uint8_t* tile = tile_s;
     typename Src::Ref nref;
     const bool have_next = src.next(ref, nref);
-    if (have_next) load(nref, raw);  // in flight during the encode
+    if constexpr (TMA) {
+      if (!bar_wait(&full[k % S], (k / S) & 1)) abort_s = 1;
+      tile = ring + (k % S) * 64 * RB;
+    } else {
+      __syncthreads();  // the previous tile's readers are done with tile_s
+#pragma unroll
+      for (int i = 0; i < NV; ++i) {
+        int idx = t + 256 * i, row = idx / VPR, cv = idx % VPR;
+        *reinterpret_cast<uint4*>(tile_s + row * RB + cv * 16) = raw[i];
+      }
+      __syncthreads();
+      if (have_next) load(nref, raw);  // in flight during the encode
+    }
 
     const QuantArgs& a = src.args(ref);
     const uint32_t Tt = (uint32_t)a.R_in, N = (uint32_t)a.C_in;
@@ -500,7 +579,21 @@ __device__ __forceinline__ void quant_cols_body(const Src& src, const QuantArgs&
     const uint32_t kb = ref.ty * 4 + kbl;
     float v[2][16];
 #pragma unroll
-    for (int e = 0; e < 16; ++e) ColTile<T>::pair(tile_s, 16 * kbl + e, np, v[0][e], v[1][e]);
+    for (int e = 0; e < 16; ++e) ColTile<T>::pair(tile, 16 * kbl + e, np, v[0][e], v[1][e]);
+    if constexpr (TMA) {
+      // every thread has its values: the slot takes the tile S ahead
+      __syncthreads();
+      if (abort_s) break;  // a tile never landed (uniform after the barrier)
+      if (t == 0 && have_i) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        tile_load(ring + (k % S) * 64 * RB, tm, (int)(iref.tx * 128), (int)(iref.ty * 64), &full[k % S], 64 * RB);
+        ++req;
+        typename Src::Ref n;
+        have_i = src.next(iref, n);
+        iref = n;
+      }
+      ++k;
+    }
     if constexpr (RHT) rht16x2(v, mask);
     bool valid[2];
 #pragma unroll
@@ -577,19 +670,29 @@ __device__ __forceinline__ void quant_cols_body(const Src& src, const QuantArgs&
     ref = nref;
     have = have_next;
   }
+  if constexpr (TMA) {
+    if (abort_s) {
+      // a wait ran out: record it, let requested tiles land (bounded) and leave
+      if (t == 0) {
+        atomicOr(a0.err, 2u);
+        for (uint32_t i = k; i < req; ++i) bar_wait(&full[i % S], (i / S) & 1);
+      }
+      return;
+    }
+  }
   if constexpr (AMAX_ONLY) cta_max_to_global(__float_as_uint(run_max), reinterpret_cast<unsigned int*>(a0.amax_accum));
 }
 
 template <typename T, bool B2D, bool SR, bool F46, bool RHT, bool AMAX_ONLY>
-__global__ void __launch_bounds__(256) k_quant_cols(QuantArgs a) {
+__global__ void __launch_bounds__(256) k_quant_cols(const __grid_constant__ CUtensorMap tm, QuantArgs a) {
   const OneTensor src(a, (uint32_t)((a.C_in + 127) / 128), (uint32_t)((a.R_in + 63) / 64));
-  quant_cols_body<T, B2D, SR, F46, RHT, AMAX_ONLY>(src, a);
+  quant_cols_body<T, B2D, SR, F46, RHT, AMAX_ONLY, true>(src, a, &tm);
 }
 
 template <typename T, bool B2D, bool SR, bool F46>
 __global__ void __launch_bounds__(256) k_quant_cols_grouped(const __grid_constant__ GroupQuant g) {
   const Groups src(g);
-  quant_cols_body<T, B2D, SR, F46, false, false>(src, g.a[0]);
+  quant_cols_body<T, B2D, SR, F46, false, false, false>(src, g.a[0]);
 }
 
 
@@ -638,13 +741,19 @@ __global__ void k_empty_scalars(float* amax, float* g) {
 // ---------------------------------------------------------------------------
 // Launchers
 // ---------------------------------------------------------------------------
+static int current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+  return dev;
+}
+
 static int num_sms() {
-  static int n = 0;
-  if (!n) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
+  static std::atomic<int> cache[64] = {};
+  const int dev = current_device();
+  int n = cache[dev].load(std::memory_order_relaxed);
+  if (n <= 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cache[dev].store(n, std::memory_order_relaxed);
   }
   return n;
 }
@@ -675,55 +784,62 @@ cudaError_t launch_amax(const void* x, bool bf16, int64_t rows, int64_t cols, in
 }
 
 // Persistent grids: as many CTAs as fit on the GPU at once (occupancy of the
-// instantiation), never more than there are tiles.
+// instantiation with its dynamic shared memory), never more than there are
+// tiles.  The resident count is cached per device in `cache`, one array per
+// kernel (each launch site owns one).
+using OccCache = std::atomic<int>[64];
 template <class K>
-static unsigned persistent_grid(K kernel, int64_t tiles) {
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 256, 0) != cudaSuccess || per_sm <= 0) per_sm = 2;
+static unsigned persistent_grid(K kernel, int64_t tiles, OccCache& cache, int smem = 0) {
+  const int dev = current_device();
+  int per_sm = cache[dev].load(std::memory_order_relaxed);
+  if (per_sm <= 0) {
+    if (smem > 48 * 1024) cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 256, smem) != cudaSuccess || per_sm <= 0)
+      per_sm = 1;
+    cache[dev].store(per_sm, std::memory_order_relaxed);
+  }
   const int64_t cap = (int64_t)num_sms() * per_sm;
   return (unsigned)(tiles < cap ? (tiles > 0 ? tiles : 1) : cap);
 }
 
 template <typename T, bool B2D, bool SR, bool F46, bool RHT, bool AO>
-static void launch_q(const QuantArgs& a, bool transpose, cudaStream_t s) {
+static cudaError_t launch_q(const QuantArgs& a, bool transpose, cudaStream_t s) {
   if (!transpose) {
     const int64_t tiles = ((a.K / 16 + 3) / 4) * ((a.R + 127) / 128);
     auto k = k_quant_rows<T, B2D, SR, F46, RHT, AO>;
-    static unsigned cap = 0;
-    if (!cap) cap = persistent_grid(k, (int64_t)1 << 40);
-    k<<<(unsigned)(tiles < cap ? tiles : cap), 256, 0, s>>>(a);
+    static OccCache occ = {};
+    k<<<persistent_grid(k, tiles, occ), 256, 0, s>>>(a);
   } else {
+    // input tiles of 64 rows x 128 columns through the TMA ring
+    CUtensorMap tm;
+    if (!make_tile_map_2d(&tm, a.x, sizeof(T) == 2, a.R_in, a.C_in, a.ld, 128, 64)) return cudaErrorInvalidValue;
     const int64_t tiles = ((a.C_in + 127) / 128) * ((a.R_in + 63) / 64);
     auto k = k_quant_cols<T, B2D, SR, F46, RHT, AO>;
-    static unsigned cap = 0;
-    if (!cap) cap = persistent_grid(k, (int64_t)1 << 40);
-    k<<<(unsigned)(tiles < cap ? tiles : cap), 256, 0, s>>>(a);
+    constexpr int smem = kColRingBytes<T>;
+    static OccCache occ = {};
+    const unsigned grid = persistent_grid(k, tiles, occ, smem);
+    k<<<grid, 256, smem, s>>>(tm, a);
   }
+  return cudaGetLastError();
 }
 
 template <typename T, bool RHT, bool AO>
-static void dispatch_opts(const QuantArgs& a, bool transpose, bool b2d, bool sr, bool f46, cudaStream_t s) {
-  if (AO) {
-    launch_q<T, false, false, false, RHT, AO>(a, transpose, s);
-    return;
-  }
+static cudaError_t dispatch_opts(const QuantArgs& a, bool transpose, bool b2d, bool sr, bool f46, cudaStream_t s) {
+  if (AO) return launch_q<T, false, false, false, RHT, AO>(a, transpose, s);
   if (b2d) {
     if (sr) {
-      if (f46) launch_q<T, true, true, true, RHT, AO>(a, transpose, s);
-      else launch_q<T, true, true, false, RHT, AO>(a, transpose, s);
-    } else {
-      if (f46) launch_q<T, true, false, true, RHT, AO>(a, transpose, s);
-      else launch_q<T, true, false, false, RHT, AO>(a, transpose, s);
+      if (f46) return launch_q<T, true, true, true, RHT, AO>(a, transpose, s);
+      return launch_q<T, true, true, false, RHT, AO>(a, transpose, s);
     }
-  } else {
-    if (sr) {
-      if (f46) launch_q<T, false, true, true, RHT, AO>(a, transpose, s);
-      else launch_q<T, false, true, false, RHT, AO>(a, transpose, s);
-    } else {
-      if (f46) launch_q<T, false, false, true, RHT, AO>(a, transpose, s);
-      else launch_q<T, false, false, false, RHT, AO>(a, transpose, s);
-    }
+    if (f46) return launch_q<T, true, false, true, RHT, AO>(a, transpose, s);
+    return launch_q<T, true, false, false, RHT, AO>(a, transpose, s);
   }
+  if (sr) {
+    if (f46) return launch_q<T, false, true, true, RHT, AO>(a, transpose, s);
+    return launch_q<T, false, true, false, RHT, AO>(a, transpose, s);
+  }
+  if (f46) return launch_q<T, false, false, true, RHT, AO>(a, transpose, s);
+  return launch_q<T, false, false, false, RHT, AO>(a, transpose, s);
 }
 
 template <typename T, bool B2D, bool SR, bool F46>
@@ -731,14 +847,12 @@ static void launch_qg(const GroupQuant& g, bool transpose, cudaStream_t s) {
   const uint32_t tiles = g.tile_start[g.count];
   if (!transpose) {
     auto k = k_quant_rows_grouped<T, B2D, SR, F46>;
-    static unsigned cap = 0;
-    if (!cap) cap = persistent_grid(k, (int64_t)1 << 40);
-    k<<<tiles < cap ? tiles : cap, 256, 0, s>>>(g);
+    static OccCache occ = {};
+    k<<<persistent_grid(k, tiles, occ), 256, 0, s>>>(g);
   } else {
     auto k = k_quant_cols_grouped<T, B2D, SR, F46>;
-    static unsigned cap = 0;
-    if (!cap) cap = persistent_grid(k, (int64_t)1 << 40);
-    k<<<tiles < cap ? tiles : cap, 256, 0, s>>>(g);
+    static OccCache occ = {};
+    k<<<persistent_grid(k, tiles, occ), 256, 0, s>>>(g);
   }
 }
 
@@ -798,20 +912,16 @@ cudaError_t launch_quantize(const QuantArgs& a, bool bf16, bool transpose, bool 
   if (a.R == 0 || a.K == 0) return cudaSuccess;
   if (bf16) {
     if (rht) {
-      if (amax_only) dispatch_opts<__nv_bfloat16, true, true>(a, transpose, false, false, false, s);
-      else dispatch_opts<__nv_bfloat16, true, false>(a, transpose, false, sr, f46, s);
-    } else {
-      dispatch_opts<__nv_bfloat16, false, false>(a, transpose, b2d, sr, f46, s);
+      if (amax_only) return dispatch_opts<__nv_bfloat16, true, true>(a, transpose, false, false, false, s);
+      return dispatch_opts<__nv_bfloat16, true, false>(a, transpose, false, sr, f46, s);
     }
-  } else {
-    if (rht) {
-      if (amax_only) dispatch_opts<float, true, true>(a, transpose, false, false, false, s);
-      else dispatch_opts<float, true, false>(a, transpose, false, sr, f46, s);
-    } else {
-      dispatch_opts<float, false, false>(a, transpose, b2d, sr, f46, s);
-    }
+    return dispatch_opts<__nv_bfloat16, false, false>(a, transpose, b2d, sr, f46, s);
   }
-  return cudaGetLastError();
+  if (rht) {
+    if (amax_only) return dispatch_opts<float, true, true>(a, transpose, false, false, false, s);
+    return dispatch_opts<float, true, false>(a, transpose, false, sr, f46, s);
+  }
+  return dispatch_opts<float, false, false>(a, transpose, b2d, sr, f46, s);
 }
 
 cudaError_t launch_empty_scalars(float* amax, float* g, cudaStream_t s) {

@@ -18,6 +18,7 @@ struct QuantArgs {
   uint8_t* scales;
   float* tdebug;        // fp32 [R][K] transformed values, or nullptr
   uint64_t seed, offset, rht_seed;
+  unsigned int* err;    // device timeout word (bounded waits of the TMA-fed encoder)
 };
 
 // Up to kQuantGroups tensors quantized by one amax launch and one encode
