@@ -186,6 +186,16 @@ __device__ __forceinline__ float rht_split_const(float m) {
   return __uint_as_float(((((__float_as_uint(m) >> 23) & 0xFFu) + 4u) << 23) | 0x400000u);
 }
 
+// Running maximum of |y| over the transformed chunks of a whole warp, exact,
+// for the amax pass (every lane of the warp calls it together; `run_max` and
+// the result are the same in every lane).  A plain fp32 butterfly comes
+// first: each output is within 2^-18 * max|x| <= 2^-18 * max|y| of the exact
+// one (four rounded stages over partial sums bounded by 16 * max|x|, and
+// max|y| >= ||x||_2 since H16 / 4 is orthogonal).  Only when a lane's bound
+// could reach the warp's exact maximum so far are that lane's chunks
+// transformed exactly (rare once the maximum has grown).
+__device__ __forceinline__ float rht16x2_absmax(float v[2][16], uint32_t sign_mask, float run_max);
+
 // v[h] <- 1/4 * H16 * diag(sigma) * v[h] for the two 16-element chunks h = 0, 1,
 // correctly rounded: every result is the fp32 value nearest the exact one.
 //   Each input is split exactly as x = hi + lo, hi = x rounded to a multiple
@@ -225,6 +235,32 @@ __device__ __forceinline__ void rht16x2(float v[2][16], uint32_t sign_mask) {
     v[0][i] = y.x;
     v[1][i] = y.y;
   }
+}
+
+__device__ __forceinline__ float rht16x2_absmax(float v[2][16], uint32_t sign_mask, float run_max) {
+  float2 p[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float sg = ((sign_mask >> i) & 1u) ? -1.0f : 1.0f;
+    p[i] = mul2_rn(make_float2(v[0][i], v[1][i]), make_float2(sg, sg));
+  }
+  wht16x2(p);
+  float m = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) m = fmaxf(m, fmaxf(fabsf(p[i].x), fabsf(p[i].y)));
+  // m / 4 is the plain maximum; the exact one is at most m / 4 * (1 + 2^-17)
+  const bool need = __fmul_rn(m, 0.25f * (1.0f + 0x1p-16f)) >= run_max;
+  if (__any_sync(0xFFFFFFFFu, need)) {
+    float e = 0.0f;
+    if (need) {
+      rht16x2(v, sign_mask);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) e = fmaxf(e, fmaxf(fabsf(v[0][i]), fabsf(v[1][i])));
+    }
+    // non-negative floats order like their bit patterns
+    run_max = fmaxf(run_max, __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, __float_as_uint(e))));
+  }
+  return run_max;
 }
 
 // --------------------------------------------------------------------------

@@ -306,9 +306,10 @@ __device__ __forceinline__ void quant_rows_body(const Src& src, const QuantArgs&
       valid[h] = r[h] < R && kb < KB;
       cur[h].unpack(v[h]);
     }
-    if constexpr (RHT) rht16x2(v, mask);
+    if constexpr (RHT && !AMAX_ONLY) rht16x2(v, mask);
     if constexpr (AMAX_ONLY) {
-      run_max = fmaxf(run_max, fmaxf(absmax16(v[0]), absmax16(v[1])));
+      if constexpr (RHT) run_max = rht16x2_absmax(v, mask, run_max);
+      else run_max = fmaxf(run_max, fmaxf(absmax16(v[0]), absmax16(v[1])));
     } else {
       float ab[2] = {absmax16(v[0]), absmax16(v[1])};
       if constexpr (B2D) {
@@ -594,13 +595,14 @@ __device__ __forceinline__ void quant_cols_body(const Src& src, const QuantArgs&
       }
       ++k;
     }
-    if constexpr (RHT) rht16x2(v, mask);
+    if constexpr (RHT && !AMAX_ONLY) rht16x2(v, mask);
     bool valid[2];
 #pragma unroll
     for (int h = 0; h < 2; ++h) valid[h] = (n0 + 2 * np + h < N) && kb < KB;
 
     if constexpr (AMAX_ONLY) {
-      run_max = fmaxf(run_max, fmaxf(absmax16(v[0]), absmax16(v[1])));
+      if constexpr (RHT) run_max = rht16x2_absmax(v, mask, run_max);
+      else run_max = fmaxf(run_max, fmaxf(absmax16(v[0]), absmax16(v[1])));
     } else {
       float ab[2] = {absmax16(v[0]), absmax16(v[1])};
       if constexpr (B2D) {
