@@ -55,7 +55,7 @@ def activations_f32(x_cpu: torch.Tensor, K: int) -> np.ndarray:
 
 
 @pytest.mark.parametrize("M", [1, 3, 4, 5, 16, 40])
-@pytest.mark.parametrize("N,K", [(1, 16), (200, 48), (256, 4096), (77, 4112)])
+@pytest.mark.parametrize("N,K", [(1, 16), (200, 48), (256, 4096), (77, 4112), (77, 4160), (33, 96), (130, 288)])
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
 def test_w4a16_random_bytes(M, N, K, out_dtype):
     q, ref = random_weight(N, K, M * 1000 + N + K)
