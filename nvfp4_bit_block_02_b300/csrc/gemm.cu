@@ -616,6 +616,11 @@ __device__ __forceinline__ void gemm_pairs(const Sched& sched, bool out_bf16, un
             tmem_ld_wait();
             NVFP4_LD_FENCE(r0);
             NVFP4_LD_FENCE(r1);
+            if (c == 2) {  // every column is in registers: release the accumulator before converting
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive_cluster(lead_accum_empty);
+            }
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               pk[16 * c + i] = pack_bf16(__fmul_rn(alpha, __uint_as_float(r0[2 * i])),
@@ -625,9 +630,11 @@ __device__ __forceinline__ void gemm_pairs(const Sched& sched, bool out_bf16, un
             }
           }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(lead_accum_empty);
+        if (!active) {  // nothing was loaded: release right away
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(lead_accum_empty);
+        }
         if (amax_out && active) {
           // producer amax of the stored BF16 values: |x| bit patterns order
           // like unsigned integers, two per word (word i = columns 2i, 2i+1);
