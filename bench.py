@@ -891,13 +891,13 @@ def _linear_fit(n1: int, t1: float, n2: int, t2: float):
     return max(t1 - b * n1, 0.0), b
 
 
-# Per workload, the slices the oracle is timed on: (X rows, W rows, GEMM output rows, GEMM output columns).  The
-# quantizations are timed at n and 2n rows (fprop: rows of X 1D and W 2D; Wgrad: columns of dY and X, transposed RHT);
-# the fp64 GEMM reference on a 2 x 2 grid of (rows, columns) = (g or 2g, c or 2c) cut from those operands.  The 1-core
-# figure divides every size by _ONE_CORE_DIV.
-_ORACLE_SLICES = {"llama8b": (2048, 3584, 1024, 1024), "llama405b": (512, 1024, 256, 512),
-                  "wgrad": (1024, 512, 512, 512), "pr1": (128, 128, 128, 128)}
-_ONE_CORE_DIV = 8
+# Oracle timing.  llama8b, wgrad and pr1 run the whole step (a few seconds on the host cores); llama405b, and the
+# 1-core figure of every fprop/wgrad workload, time slices and extrapolate: per workload (X rows, W rows, GEMM
+# output rows, GEMM output columns) at all cores; the 1-core figure divides the sizes by _ONE_CORE_DIV.
+_FULL_STEP = ("llama8b", "wgrad", "pr1")
+_ORACLE_SLICES = {"llama8b": (2048, 3584, 1024, 2048), "llama405b": (512, 1024, 512, 2048),
+                  "wgrad": (1024, 512, 1024, 1024), "pr1": (128, 128, 128, 128)}
+_ONE_CORE_DIV = 4
 
 
 def _time(fn):
@@ -907,17 +907,18 @@ def _time(fn):
 
 
 def _oracle_step(workload: str, X, W, div: int = 1) -> dict:
-    """Time the oracle, as it stands, on bounded slices of one step and
-    extrapolate each part linearly to the whole step.
+    """Time the oracle, as it stands, on one step of the workload.
 
-    Each part (quantize X, quantize W, the fp64 GEMM reference) is timed at
-    two sizes n and 2n; t(n) = a + b*n separates the fixed cost a (charged
-    once per step) from the per-unit cost b, so the extrapolation never
-    multiplies a fixed cost.  The GEMM part runs its output rows against the
-    2n-row W slice and is scaled by N / (that slice).  MoE times one whole
-    expert (scaled to 64), W4A16 one whole layer (scaled to 8): both are the
-    step's own repeated unit.  Returns the extrapolated step seconds, the
-    seconds actually spent, and the per-part fits."""
+    Whole step (llama8b, wgrad, pr1 at all cores): quantize both operands and
+    the fp64 GEMM reference, no extrapolation.  MoE times one whole expert
+    (scaled to 64), W4A16 one whole layer (scaled to 8): the step's own
+    repeated unit.  Otherwise slices, each part extrapolated separately:
+    every quantization is timed at two sizes n and 2n and fit as a + b*n (the
+    fixed cost a is charged once); the GEMM reference is timed on a block of
+    output rows and columns, and its operand conversions (oracle.exact_values
+    of the A rows and of the B rows) are timed on their own, so that the
+    products' cost per output is separated from the per-row and per-column
+    conversion costs before each is scaled to the whole step."""
     import oracle
     c = WORKLOADS[workload]
     M, N = c["M"], c["N"]
@@ -934,49 +935,49 @@ def _oracle_step(workload: str, X, W, div: int = 1) -> dict:
         return {"step_s": c["E"] * t, "spent_s": t,
                 "parts": {"quantize_w_s": round(tw, 4), "quantize_x_s": round(tx, 4), "gemm_s": round(tg, 4)},
                 "work": f"one whole expert (W_e^T Four-over-Six, X_e, GEMM {c['M']}x{N}x{c['K']}), x{c['E']}"}
-    rx, rw, rg, rc = (max(1, v // div) for v in _ORACLE_SLICES[workload])
-    if workload == "pr1":   # the whole step is small: time it as it is
-        tq1, qa = _time(lambda: oracle.quantize(X))
-        tq2, qb = _time(lambda: oracle.quantize(W))
-        tg, _ = _time(lambda: oracle.gemm_reference(qa, qb))
-        t = tq1 + tq2 + tg
-        return {"step_s": t, "spent_s": t, "parts": {"quantize_a_s": tq1, "quantize_b_s": tq2, "gemm_s": tg},
-                "work": "the whole step (no extrapolation)"}
     if workload == "wgrad":
         qa_fn = lambda n: oracle.quantize(np.ascontiguousarray(X[:, :n]), transpose=True, rht=True, stochastic=True,
                                           seed=1, rht_seed=1)
         qb_fn = lambda n: oracle.quantize(np.ascontiguousarray(W[:, :n]), transpose=True, rht=True, rht_seed=1)
+        n_a, n_b = X.shape[1], W.shape[1]
     else:
         qa_fn = lambda n: oracle.quantize(X[:n])
-        qb_fn = lambda n: oracle.quantize(W[:n], block2d=True)
+        qb_fn = lambda n: oracle.quantize(W[:n], block2d=workload != "pr1")
+        n_a, n_b = X.shape[0], W.shape[0]
+    if div == 1 and workload in _FULL_STEP:
+        ta, qa = _time(lambda: qa_fn(n_a))
+        tb, qb = _time(lambda: qb_fn(n_b))
+        tg, _ = _time(lambda: oracle.gemm_reference(qa, qb))
+        t = ta + tb + tg
+        return {"step_s": t, "spent_s": t,
+                "parts": {"quantize_a_s": round(ta, 3), "quantize_b_s": round(tb, 3), "gemm_reference_s": round(tg, 3)},
+                "work": "the whole step (both quantizations and the full fp64 GEMM reference), no extrapolation"}
+    rx, rw, rg, rc = (max(1, v // div) for v in _ORACLE_SLICES[workload])
     ta1, _ = _time(lambda: qa_fn(rx))
     ta2, qa = _time(lambda: qa_fn(2 * rx))
     tb1, _ = _time(lambda: qb_fn(rw))
     tb2, qb = _time(lambda: qb_fn(2 * rw))
     fa, fb = _linear_fit(rx, ta1, 2 * rx, ta2), _linear_fit(rw, tb1, 2 * rw, tb2)
-    # GEMM reference: t(g, c) = c0 + cA*g + cB*c + cAB*g*c (operand conversions and the products), from the
-    # 2 x 2 grid of output rows g and output columns c
-    cols = lambda c: oracle.Quantized(qb.codes[:c], qb.scales[:c], qb.amax, qb.g, None, None, c, qb.K)
-    tg = {(g, c): _time(lambda: oracle.gemm_reference(qa, cols(c), rows=np.arange(g)))[0]
-          for g in (rg, 2 * rg) for c in (rc, 2 * rc)}
-    t11, t21, t12, t22 = tg[rg, rc], tg[2 * rg, rc], tg[rg, 2 * rc], tg[2 * rg, 2 * rc]
-    cab = max((t22 - t21 - t12 + t11) / (rg * rc), 0.0)
-    ca = max((t21 - t11) / rg - cab * rc, 0.0)
-    cb = max((t12 - t11) / rc - cab * rg, 0.0)
-    c0 = max(t11 - ca * rg - cb * rc - cab * rg * rc, 0.0)
-    t_gemm = c0 + ca * M + cb * N + cab * M * N
+    rg, rc = min(rg, qa.R), min(rc, qb.R)
+    qbc = oracle.Quantized(qb.codes[:rc], qb.scales[:rc], qb.amax, qb.g, None, None, rc, qb.K)
+    qag = oracle.Quantized(qa.codes[:rg], qa.scales[:rg], qa.amax, qa.g, None, None, rg, qa.K)
+    tg, _ = _time(lambda: oracle.gemm_reference(qag, qbc))
+    tca, _ = _time(lambda: oracle.exact_values(qag.codes, qag.scales, qag.g))
+    tcb, _ = _time(lambda: oracle.exact_values(qbc.codes, qbc.scales, qbc.g))
+    prod = max(tg - tca - tcb, 0.0)
+    t_gemm = tca * M / rg + tcb * N / rc + prod * (M / rg) * (N / rc)
     step = (fa[0] + fa[1] * M) + (fb[0] + fb[1] * N) + t_gemm
-    spent = ta1 + ta2 + tb1 + tb2 + sum(tg.values())
-    parts = {name: {"fixed_s": round(a, 5), "per_unit_us": round(b * 1e6, 4), "fixed_frac_at_n": round(a / t, 4)}
-             for name, (a, b), t in (("quantize_a", fa, ta1), ("quantize_b", fb, tb1))}
-    parts["gemm"] = {"fixed_s": round(c0, 5), "per_row_us": round(ca * 1e6, 3), "per_col_us": round(cb * 1e6, 3),
-                     "per_output_ns": round(cab * 1e9, 3), "whole_step_s": round(t_gemm, 3),
-                     "products_frac_at_sample": round(cab * 4 * rg * rc / t22, 4)}
+    spent = ta1 + ta2 + tb1 + tb2 + tg + tca + tcb
+    parts = {name: {"fixed_s": round(a_, 5), "per_unit_us": round(b_ * 1e6, 4), "fixed_frac_at_n": round(a_ / t_, 4)}
+             for name, (a_, b_), t_ in (("quantize_a", fa, ta1), ("quantize_b", fb, tb1))}
+    parts["gemm"] = {"block": [rg, rc], "block_s": round(tg, 4), "convert_a_rows_s": round(tca, 4),
+                     "convert_b_rows_s": round(tcb, 4), "products_per_output_ns": round(prod / (rg * rc) * 1e9, 3),
+                     "whole_step_s": round(t_gemm, 3)}
     unit = "columns" if workload == "wgrad" else "rows"
     return {"step_s": step, "spent_s": spent, "parts": parts,
-            "work": (f"quantize A {unit} [0,{rx}) and [0,{2 * rx}), B {unit} [0,{rw}) and [0,{2 * rw}) (each fit as "
-                     f"a + b*n); fp64 GEMM reference on output blocks of {rg} or {2 * rg} rows x {rc} or {2 * rc} "
-                     f"columns (fit as c0 + cA*rows + cB*cols + cAB*rows*cols); extrapolated to the whole step")}
+            "work": (f"extrapolated: quantize A {unit} [0,{rx}) and [0,{2 * rx}), B {unit} [0,{rw}) and [0,{2 * rw}) "
+                     f"(each fit as a + b*n); fp64 GEMM reference on a {rg} x {rc} output block with its operand "
+                     f"conversions timed apart; each part scaled to the whole step")}
 
 
 def _set_threads(n: int | None):
@@ -1005,13 +1006,13 @@ def cpu_baseline(workload: str):
     r1 = None
     if workload in _ORACLE_SLICES:   # MoE and W4A16 time a whole expert / layer: no 1-core run of that size
         lim = _set_threads(1)
-        r1 = _oracle_step(workload, X, W, div=1 if workload == "pr1" else _ONE_CORE_DIV)
+        r1 = _oracle_step(workload, X, W, div=_ONE_CORE_DIV)
         if lim is not None:
             lim.restore_original_limits()
         _set_threads(None)
     flops = _flops(workload)
     out = {"value": round(flops / r["step_s"] / 1e12, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-           "sample": r["work"], "extrapolated": workload != "pr1",
+           "sample": r["work"], "extrapolated": workload not in _FULL_STEP,
            "extrapolated_step_seconds": round(r["step_s"], 3), "sample_seconds": round(r["spent_s"], 2),
            "parts": r["parts"]}
     if r1 is not None:
@@ -1047,7 +1048,8 @@ def run_reference(args):
                          "as a + b*n at two sizes); ms_per_step is the time the sample itself took"),
             "extrapolated_step_ms": round(t_full * 1e3, 1),
             "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                             "sample": "per step: " + runs[0]["work"], "extrapolated": args.workload != "pr1"},
+                             "sample": "per step: " + runs[0]["work"],
+                             "extrapolated": args.workload not in _FULL_STEP},
             "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 

@@ -44,3 +44,22 @@ def test_dequantize_round_trip_of_grid_values():
     nv.sync_check()
     ref = oracle_quantize_like(x)
     assert (y.cpu().numpy() == oracle.dequantize(ref.codes, ref.scales, ref.g)).all()
+
+
+def test_dequantize_llama8b_weight_sampled():
+    """The Llama-3-8B MLP weight (14336 x 4096, 2D blocks) decoded to BF16 in
+    full on the GPU; sampled rows bit-exact with the oracle's decode of the
+    same codes and scales rounded to BF16."""
+    wl = synthetic.llama8b_fprop()
+    q = nv.quantize(wl.tensors["W"].cuda(), block="2d")
+    y = nv.dequantize(q, torch.bfloat16)
+    nv.sync_check()
+    rows = np.sort(np.random.default_rng(9).choice(14336, 256, replace=False))
+    codes = q.codes.cpu().numpy()[rows]
+    KB = 4096 // 16
+    r = rows.astype(np.int64)[:, None]
+    kb = np.arange(KB, dtype=np.int64)[None, :]
+    phys = q.scales.cpu().numpy()
+    scales = phys[((r >> 7) * (KB // 4) + (kb >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (kb & 3)]
+    yr = oracle.dequantize(codes, scales, float(q.global_scale.cpu()[0]))
+    assert torch.equal(y[torch.from_numpy(rows).cuda()].cpu(), torch.from_numpy(yr).to(torch.bfloat16))
