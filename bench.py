@@ -712,7 +712,8 @@ def run_moe(args, rank, world, local_rank):
         },
         "roofline": {"bound": "hbm", "kernel": "k_gemm_grouped (64 experts, one launch)",
                      "achieved": round(g_gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-                     "frac": round(g_gbs / pk["hbm_gbs"], 4), "traffic": None,
+                     "frac": round(g_gbs / pk["hbm_gbs"], 4),
+                     "traffic": ncu_traffic("k_gemm_grouped", source_hash("gemm.cu", "gemm.h"), "moe"),
                      "algorithmic_bytes_per_launch": gbytes, "peak_source": f"{pk_src} copy bandwidth"},
         "e2e": {"value": round(world * flops / e2e_s / 1e12, 3), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": int(w_h.numel() * 2 + x_h.numel() * 2),
