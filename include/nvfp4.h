@@ -48,7 +48,7 @@ typedef enum {
   NVFP4_ERR_UNSUPPORTED_SHAPE = 2, /* shape rule broken (see each function) */
   NVFP4_ERR_MISALIGNED = 3,        /* pointer or leading dimension not 16-byte aligned */
   NVFP4_ERR_CUDA = 4,              /* a CUDA runtime/driver call failed */
-  NVFP4_ERR_TIMEOUT = 5            /* a GEMM pipeline wait ran out (reported by nvfp4_sync_check) */
+  NVFP4_ERR_TIMEOUT = 5            /* a pipeline wait (GEMM, transposed encoder) ran out; nvfp4_sync_check */
 } nvfp4_status;
 
 typedef enum { NVFP4_F32 = 0, NVFP4_BF16 = 1 } nvfp4_dtype;
@@ -294,13 +294,31 @@ nvfp4_status nvfp4_gemm_quantize(const nvfp4_tensor* A, const nvfp4_tensor* B, c
 nvfp4_status nvfp4_gemm_grouped(int count, const nvfp4_tensor* A, const nvfp4_tensor* B, void* const* D,
                                 nvfp4_dtype dt, void* stream);
 
-/* Synchronise `stream`, then report a pending CUDA error, or a GEMM pipeline
- * timeout recorded on the current device.  The timeout word is one per
- * device, shared by every GEMM launched on it from any stream or thread: it
- * is read and cleared in one atomic exchange ordered on `stream`, so a timeout
- * is reported once, by the first nvfp4_sync_check that follows it, and with
- * GEMMs in flight on other streams it may belong to one of those. */
+/* Synchronise `stream`, then report a pending CUDA error, or a pipeline
+ * timeout recorded on the current device.  Every mbarrier wait of the GEMMs
+ * and of the TMA-fed transposed encoder is bounded (2 s); on expiry the CTA
+ * records it in a device word (bit 0: GEMM, bit 1: encoder), lets its copies
+ * in flight land, frees its tensor memory and returns, leaving its outputs
+ * undefined.  The word is one per device, shared by every kernel launched on
+ * it from any stream or thread: it is read and cleared in one atomic exchange
+ * ordered on `stream`, so a timeout is reported once, by the first
+ * nvfp4_sync_check that follows it, and with kernels in flight on other
+ * streams it may belong to one of those. */
 nvfp4_status nvfp4_sync_check(void* stream);
+
+/* Failure-detection test support; no operation of the method.  Arms the next
+ * launch this process makes of
+ *   op 1: the plain GEMM (nvfp4_gemm, nvfp4_gemm_amax), or
+ *   op 2: the TMA-fed transposed encoder (the first kernel of a transposed
+ *         nvfp4_quantize / nvfp4_rht_quantize that reads through its ring),
+ * so that the first pipeline barrier of every CTA pair (op 1) or CTA (op 2)
+ * waits for 16 bytes that no copy delivers.  The bounded wait on it runs out
+ * after limit_ns and the kernel takes the timeout path above; the next
+ * nvfp4_sync_check reports NVFP4_ERR_TIMEOUT and the device stays usable.
+ * limit_ns in [1 ms, 2 s].  Arming is process-wide and consumed by the first
+ * launch it matches; limit_ns = 0 disarms.  NVFP4_ERR_INVALID_ARG for another
+ * op or limit. */
+nvfp4_status nvfp4_test_expire_next_wait(int op, uint64_t limit_ns);
 
 /* Human-readable status name (static string). */
 const char* nvfp4_status_string(nvfp4_status s);

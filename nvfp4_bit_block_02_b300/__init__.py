@@ -81,9 +81,10 @@ def lib() -> ctypes.CDLL:
                                          ctypes.POINTER(ctypes.c_void_p), ctypes.c_int, P]
         L.nvfp4_w4a16_gemm.argtypes = [P, ctypes.c_int, I64, I64, ctypes.POINTER(CTensor), P, ctypes.c_int, I64, P]
         L.nvfp4_sync_check.argtypes = [P]
+        L.nvfp4_test_expire_next_wait.argtypes = [ctypes.c_int, ctypes.c_uint64]
         for fn in ("nvfp4_amax", "nvfp4_quantize", "nvfp4_quantize_grouped", "nvfp4_rht_quantize", "nvfp4_dequantize",
                    "nvfp4_transpose_2d", "nvfp4_gemm", "nvfp4_gemm_amax", "nvfp4_gemm_quantize", "nvfp4_gemm_grouped", "nvfp4_w4a16_gemm",
-                   "nvfp4_sync_check"):
+                   "nvfp4_sync_check", "nvfp4_test_expire_next_wait"):
             getattr(L, fn).restype = ctypes.c_int
         L.nvfp4_status_string.argtypes = [ctypes.c_int]
         L.nvfp4_status_string.restype = ctypes.c_char_p
@@ -321,6 +322,17 @@ def w4a16_gemm(x: torch.Tensor, w: NVFP4Tensor, out_dtype=torch.bfloat16, out: t
 
 
 def sync_check(stream=None):
-    """Synchronise the stream and raise on a pending CUDA error or a GEMM
-    pipeline timeout."""
+    """Synchronise the stream and raise on a pending CUDA error or a pipeline
+    timeout (GEMM or transposed encoder)."""
     _check(lib().nvfp4_sync_check(_stream(stream)), "nvfp4_sync_check")
+
+
+TEST_GEMM, TEST_TRANSPOSED_ENCODER = 1, 2
+
+
+def test_expire_next_wait(op: int, limit_ns: int):
+    """nvfp4_test_expire_next_wait: failure-detection test support.  The next
+    launch of the plain GEMM (op 1) or of the TMA-fed transposed encoder
+    (op 2) waits on a barrier that never completes, so its bounded wait runs
+    out after limit_ns and the next sync_check raises NVFP4_ERR_TIMEOUT."""
+    _check(lib().nvfp4_test_expire_next_wait(op, limit_ns), "nvfp4_test_expire_next_wait")

@@ -408,7 +408,16 @@ nvfp4_status nvfp4_sync_check(void* stream) {
   unsigned int v = 0;
   e = nvfp4::take_device_error(reinterpret_cast<cudaStream_t>(stream), &v);
   if (e != cudaSuccess) return cuda_fail(e, "read device error word");
-  if (v) return fail(NVFP4_ERR_TIMEOUT, "a GEMM pipeline wait exceeded its limit");
+  if (v) return fail(NVFP4_ERR_TIMEOUT, (v & 1u) ? "a GEMM pipeline wait exceeded its limit"
+                                                  : "a transposed-encoder pipeline wait exceeded its limit");
+  return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_test_expire_next_wait(int op, uint64_t limit_ns) {
+  if (op != 1 && op != 2) return fail(NVFP4_ERR_INVALID_ARG, "op must be 1 (GEMM) or 2 (transposed encoder)");
+  if (limit_ns != 0 && (limit_ns < 1000000ull || limit_ns > 2000000000ull))
+    return fail(NVFP4_ERR_INVALID_ARG, "limit_ns must be 0 or in [1e6, 2e9]");
+  nvfp4::arm_wait_expiry(op, limit_ns);
   return NVFP4_OK;
 }
 

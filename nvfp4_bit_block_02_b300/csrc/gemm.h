@@ -36,6 +36,11 @@ struct GemmArgs {
   unsigned int* err;
   unsigned int* amax_out;  // nullable: atomicMax of |D| (as stored) over the output, float bits
   GemmQuantOut q;          // used by the quantizing variant only
+  // Failure-detection test only (0 in every normal launch): extra bytes the
+  // leader CTA of each pair expects on its first stage's barrier, which no
+  // copy delivers, and the wait limit in ns (0: the default limit).
+  unsigned int hold_tx;
+  unsigned long long wait_ns;
 };
 
 constexpr int kGroupsPerLaunch = 64;
@@ -65,6 +70,13 @@ bool make_tile_map_2d(CUtensorMap* m, const void* base, bool bf16, int64_t rows,
 // Read and clear the current device's timeout word in one atomic exchange
 // (ordered on `s`), then synchronise `s` and return the value read.
 cudaError_t take_device_error(cudaStream_t s, unsigned int* value);
+// Failure-detection test support: arm the next launch of the plain GEMM
+// (op 1) or of the TMA-fed transposed encoder (op 2) made by this process so
+// that one of its pipeline barriers is never completed and the bounded wait
+// on it runs out after limit_ns.  take_armed_wait returns the armed limit
+// for `op` and disarms it (0 when not armed).
+void arm_wait_expiry(int op, unsigned long long limit_ns);
+unsigned long long take_armed_wait(int op);
 int gemm_tile_m();
 int gemm_tile_n();
 cudaError_t launch_gemm(const GemmOperand& A, const GemmOperand& B, void* D, int64_t ldd, bool out_bf16, cudaStream_t s,

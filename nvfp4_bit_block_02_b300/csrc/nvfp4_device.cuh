@@ -48,19 +48,6 @@ __device__ __forceinline__ float e4m3_value(uint32_t b) {
   return __low2float(*reinterpret_cast<const __half2*>(&h));
 }
 
-// Magnitude of E2M1 index m (0..7): 0, .5, 1, 1.5, 2, 3, 4, 6 (exact bits).
-__device__ __forceinline__ float e2m1_mag(uint32_t m) {
-  uint32_t hi = m >> 1;
-  uint32_t bits = ((126u + hi) << 23) | ((hi ? (m & 1u) : 0u) << 22);
-  return m ? __uint_as_float(bits) : 0.0f;
-}
-
-// Signed value of a 4-bit code.
-__device__ __forceinline__ float e2m1_value(uint32_t code) {
-  float v = e2m1_mag(code & 7u);
-  return (code & 8u) ? -v : v;
-}
-
 // Stochastic rounding of a = |q| to an E2M1 magnitude index with a 16-bit
 // uniform number u, given as nu = 65535 - u: neighbours lo <= a < hi on the
 // grid, frac = (a - lo) / (hi - lo), round up iff u < fl(frac * 65536);
@@ -78,6 +65,56 @@ __device__ __forceinline__ uint32_t e2m1_sr_index(float a, uint32_t nu) {
   const uint32_t tl = __float_as_uint(__fmaf_ru(a, 131072.0f, 8388608.0f)) - 0x4B000000u;
   const uint32_t tg = (__float_as_uint(a) - 0x3F000000u + 63u) >> 6;
   return min(((a < 1.0f ? tl : tg) + nu) >> 16, 7u);
+}
+
+// Decode: y = fl(fl(value(code) * s) * g), two codes at a time.  The values
+// of a code byte come from one hardware conversion to f16x2 (every E2M1 value
+// is an f16); value * s is formed in f32 by a mixed-precision fma with f16
+// multiplicands, exact because every |value * s| lies in [2^-10, 2688] with at
+// most 6 significant bits (adding -0 keeps the sign of a zero product); the
+// product with g is one packed IEEE multiply.
+//
+// (s, s) in f16 from an E4M3 scale byte with its sign bit clear (exact).
+__device__ __forceinline__ uint32_t e4m3_f16x2_splat(uint32_t b) {
+  uint32_t h;
+  asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(h) : "r"(b * 0x101u));
+  return h;
+}
+// The 16 codes of a block (byte p = codes 2p, 2p+1, low nibble first) as 8
+// f16x2 words of their values; the vector move hands each byte to its
+// conversion without a shift.
+__device__ __forceinline__ void e2m1x16_f16x2(uint2 c, uint32_t h[8]) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3, b4, b5, b6, b7;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %8;\n\t"
+      "mov.b32 {b4, b5, b6, b7}, %9;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %4, b4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %5, b5;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %6, b6;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %7, b7;\n\t}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3]), "=r"(h[4]), "=r"(h[5]), "=r"(h[6]), "=r"(h[7])
+      : "r"(c.x), "r"(c.y));
+}
+// fl(fl(v * s) * g) for the two values of f16x2 word h, s from e4m3_f16x2_splat.
+__device__ __forceinline__ float2 decode_pair(uint32_t h, uint32_t s2, float2 g2) {
+  float lo, hi;
+  asm("{\n\t.reg .b16 v0, v1, sc, sd;\n\t"
+      "mov.b32 {v0, v1}, %2;\n\t"
+      "mov.b32 {sc, sd}, %3;\n\t"
+      "fma.rn.f32.f16 %0, v0, sc, 0f80000000;\n\t"
+      "fma.rn.f32.f16 %1, v1, sc, 0f80000000;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(h), "r"(s2));
+  float2 p;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(p.x), "=f"(p.y)
+      : "f"(lo), "f"(hi), "f"(g2.x), "f"(g2.y));
+  return p;
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -315,24 +352,35 @@ __device__ __forceinline__ uint2 encode16(const float v[16], float rcp, const ui
   }
 }
 
-// The two E2M1 codes of byte `b` (low nibble first) -> their values in fp32,
-// exact (every E2M1 value is an f16): one hardware conversion per pair.
-__device__ __forceinline__ float2 e2m1x2_values(uint32_t b) {
-  uint32_t h;
-  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(h) : "r"(b));
-  return __half22float2(*reinterpret_cast<const __half2*>(&h));
+// value * s for the two values of f16x2 word h (s from e4m3_f16x2_splat),
+// exact in f32: mixed-precision fma with f16 multiplicands, adding -0.
+__device__ __forceinline__ float2 scaled_pair(uint32_t h, uint32_t s2) {
+  float2 r;
+  asm("{\n\t.reg .b16 v0, v1, sc, sd;\n\t"
+      "mov.b32 {v0, v1}, %2;\n\t"
+      "mov.b32 {sc, sd}, %3;\n\t"
+      "fma.rn.f32.f16 %0, v0, sc, 0f80000000;\n\t"
+      "fma.rn.f32.f16 %1, v1, sc, 0f80000000;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "r"(h), "r"(s2));
+  return r;
 }
 
 // Squared error of 16 encoded values against their decode fl(fl(v*s)*g),
-// pairwise summed: ((e0+e1)+(e2+e3)) + ... over the 16 in order.  Scalar
-// IEEE operations throughout; the codes are decoded two at a time.
-__device__ __forceinline__ float block_sq_err16(const float v[16], uint2 codes, float s, float g) {
+// pairwise summed: ((e0+e1)+(e2+e3)) + ... over the 16 in order; s is the
+// E4M3 scale byte.  Scalar IEEE operations with explicit rounding (a packed
+// product feeding a packed difference was seen to change the result on the
+// B300 for a few near-tie blocks, consistent with the two being fused).
+__device__ __forceinline__ float block_sq_err16(const float v[16], uint2 codes, uint32_t sbyte, float g) {
+  const uint32_t s2 = e4m3_f16x2_splat(sbyte & 0x7Fu);
+  uint32_t h[8];
+  e2m1x16_f16x2(codes, h);
   float e[16];
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    const float2 val = e2m1x2_values((j < 4 ? codes.x : codes.y) >> (8 * (j & 3)));
-    const float d0 = __fsub_rn(v[2 * j], __fmul_rn(__fmul_rn(val.x, s), g));
-    const float d1 = __fsub_rn(v[2 * j + 1], __fmul_rn(__fmul_rn(val.y, s), g));
+    const float2 vs = scaled_pair(h[j], s2);
+    const float d0 = __fsub_rn(v[2 * j], __fmul_rn(vs.x, g));
+    const float d1 = __fsub_rn(v[2 * j + 1], __fmul_rn(vs.y, g));
     e[2 * j] = __fmul_rn(d0, d0);
     e[2 * j + 1] = __fmul_rn(d1, d1);
   }

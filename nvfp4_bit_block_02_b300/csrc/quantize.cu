@@ -328,25 +328,24 @@ __device__ __forceinline__ void quant_rows_body(const Src& src, const QuantArgs&
       }
       uint2 codes[2], c4[2];
       uint32_t sbyte[2], b4[2];
-      float s6[2], s4[2];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         uint32_t u[16];
         if constexpr (SR) sr_draws16(a.seed, a.offset, (uint64_t)r[h] * (uint64_t)a.K + kb * 16, u);
-        float r6;
-        sbyte[h] = block_scale(ab[h], g6, g, s6[h], r6);
+        float s6, r6;
+        sbyte[h] = block_scale(ab[h], g6, g, s6, r6);
         codes[h] = encode16<SR>(v[h], r6, u);
         if constexpr (F46) {
-          float r4;
-          b4[h] = block_scale(ab[h], g4, g, s4[h], r4);
+          float s4, r4;
+          b4[h] = block_scale(ab[h], g4, g, s4, r4);
           c4[h] = encode16<SR>(v[h], r4, u);
         }
       }
       if constexpr (F46) {
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          float e6 = block_sq_err16(v[h], codes[h], s6[h], g);
-          float e4 = block_sq_err16(v[h], c4[h], s4[h], g);
+          float e6 = block_sq_err16(v[h], codes[h], sbyte[h], g);
+          float e4 = block_sq_err16(v[h], c4[h], b4[h], g);
           if constexpr (B2D) {
 #pragma unroll
             for (int o = 4; o <= 16; o <<= 1) {
@@ -456,8 +455,8 @@ __device__ __forceinline__ bool bar_test(uint64_t* b, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait (2 s of global time): false on timeout.
-__device__ __forceinline__ bool bar_wait(uint64_t* b, uint32_t parity) {
+// Bounded wait (`limit` ns of global time): false on timeout.
+__device__ __forceinline__ bool bar_wait(uint64_t* b, uint32_t parity, unsigned long long limit) {
   if (bar_test(b, parity)) return true;
   unsigned long long t0, t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
@@ -465,7 +464,7 @@ __device__ __forceinline__ bool bar_wait(uint64_t* b, uint32_t parity) {
     if (bar_test(b, parity)) return true;
     if ((it & 63u) == 0) {
       asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-      if (t - t0 > 2000000000ull) return false;
+      if (t - t0 > limit) return false;
     }
   }
 }
@@ -480,8 +479,11 @@ __device__ __forceinline__ void tile_load(void* dst, const CUtensorMap* tm, int 
 }
 
 // TMA (single tensor, tm != nullptr) or register prefetch (grouped tensors).
+// hold_tx and wait_ns: the failure-detection test's withheld bytes on each
+// CTA's first tile and its wait limit (both 0 in normal launches: 2 s).
 template <typename T, bool B2D, bool SR, bool F46, bool RHT, bool AMAX_ONLY, bool TMA, class Src>
-__device__ __forceinline__ void quant_cols_body(const Src& src, const QuantArgs& a0, const CUtensorMap* tm = nullptr) {
+__device__ __forceinline__ void quant_cols_body(const Src& src, const QuantArgs& a0, const CUtensorMap* tm = nullptr,
+                                                uint32_t hold_tx = 0, unsigned long long wait_ns = 0) {
   constexpr int RB = ColTile<T>::kRowBytes;
   constexpr int VPR = RB / 16;                  // 16-byte vectors per tile row
   constexpr int NV = TMA ? 1 : (64 * VPR) / 256;  // vectors per thread (register path)
@@ -530,6 +532,7 @@ __device__ __forceinline__ void quant_cols_body(const Src& src, const QuantArgs&
   [[maybe_unused]] bool have_i = have;
   [[maybe_unused]] uint32_t k = 0;    // this CTA's tile counter (TMA ring position)
   [[maybe_unused]] uint32_t req = 0;  // (thread 0) tiles requested so far
+  [[maybe_unused]] const unsigned long long limit = wait_ns ? wait_ns : 2000000000ull;
   if constexpr (TMA) {
     if (t == 0) {
       abort_s = 0;
@@ -538,7 +541,8 @@ __device__ __forceinline__ void quant_cols_body(const Src& src, const QuantArgs&
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
       iref = ref;
       for (int i = 0; i < S && have_i; ++i) {
-        tile_load(ring + i * 64 * RB, tm, (int)(iref.tx * 128), (int)(iref.ty * 64), &full[i], 64 * RB);
+        tile_load(ring + i * 64 * RB, tm, (int)(iref.tx * 128), (int)(iref.ty * 64), &full[i],
+                  64 * RB + (i == 0 ? hold_tx : 0u));
         ++req;
         typename Src::Ref n;
         have_i = src.next(iref, n);
@@ -554,7 +558,7 @@ __device__ __forceinline__ void quant_cols_body(const Src& src, const QuantArgs&
     typename Src::Ref nref;
     const bool have_next = src.next(ref, nref);
     if constexpr (TMA) {
-      if (!bar_wait(&full[k % S], (k / S) & 1)) abort_s = 1;
+      if (!bar_wait(&full[k % S], (k / S) & 1, limit)) abort_s = 1;
       tile = ring + (k % S) * 64 * RB;
     } else {
       __syncthreads();  // the previous tile's readers are done with tile_s
@@ -614,7 +618,7 @@ __device__ __forceinline__ void quant_cols_body(const Src& src, const QuantArgs&
       }
       uint2 codes[2], c4[2];
       uint32_t sbyte[2], b4[2];
-      float e6[2], e4[2], s6v[2], s4v[2];
+      float e6[2], e4[2];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const uint32_t n = n0 + 2 * np + h;
@@ -624,17 +628,16 @@ __device__ __forceinline__ void quant_cols_body(const Src& src, const QuantArgs&
         sbyte[h] = block_scale(ab[h], g6, g, s6, r6);
         codes[h] = encode16<SR>(v[h], r6, u);
         if constexpr (F46) {
-          float r4;
-          b4[h] = block_scale(ab[h], g4, g, s4v[h], r4);
+          float s4, r4;
+          b4[h] = block_scale(ab[h], g4, g, s4, r4);
           c4[h] = encode16<SR>(v[h], r4, u);
-          s6v[h] = s6;
         }
       }
       if constexpr (F46) {
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          e6[h] = block_sq_err16(v[h], codes[h], s6v[h], g);
-          e4[h] = block_sq_err16(v[h], c4[h], s4v[h], g);
+          e6[h] = block_sq_err16(v[h], codes[h], sbyte[h], g);
+          e4[h] = block_sq_err16(v[h], c4[h], b4[h], g);
         }
         if constexpr (B2D) {
           // tile rows 2p, 2p+1 are this thread's pair; then pairs of pairs ...
@@ -677,7 +680,7 @@ __device__ __forceinline__ void quant_cols_body(const Src& src, const QuantArgs&
       // a wait ran out: record it, let requested tiles land (bounded) and leave
       if (t == 0) {
         atomicOr(a0.err, 2u);
-        for (uint32_t i = k; i < req; ++i) bar_wait(&full[i % S], (i / S) & 1);
+        for (uint32_t i = k; i < req; ++i) bar_wait(&full[i % S], (i / S) & 1, limit);
       }
       return;
     }
@@ -686,9 +689,10 @@ __device__ __forceinline__ void quant_cols_body(const Src& src, const QuantArgs&
 }
 
 template <typename T, bool B2D, bool SR, bool F46, bool RHT, bool AMAX_ONLY>
-__global__ void __launch_bounds__(256) k_quant_cols(const __grid_constant__ CUtensorMap tm, QuantArgs a) {
+__global__ void __launch_bounds__(256) k_quant_cols(const __grid_constant__ CUtensorMap tm, QuantArgs a, uint32_t hold_tx,
+                                                   unsigned long long wait_ns) {
   const OneTensor src(a, (uint32_t)((a.C_in + 127) / 128), (uint32_t)((a.R_in + 63) / 64));
-  quant_cols_body<T, B2D, SR, F46, RHT, AMAX_ONLY, true>(src, a, &tm);
+  quant_cols_body<T, B2D, SR, F46, RHT, AMAX_ONLY, true>(src, a, &tm, hold_tx, wait_ns);
 }
 
 template <typename T, bool B2D, bool SR, bool F46>
@@ -705,31 +709,46 @@ template <typename TO>
 __global__ void __launch_bounds__(256) k_dequant(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales,
                                                  const float* __restrict__ gptr, int64_t R, int64_t K, TO* __restrict__ y) {
   const float g = *gptr;
-  const int64_t KB = K / 16, nka = (KB + 3) / 4, nblk = R * KB;
-  for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < nblk; b += (int64_t)gridDim.x * blockDim.x) {
-    int64_t r = b / KB, kb = b % KB;
-    uint2 c = *reinterpret_cast<const uint2*>(codes + r * (K / 2) + kb * 8);
-    float s = e4m3_value(scales[sf_offset(r, kb, nka)] & 0x7Fu);
-    float o[16];
+  const float2 g2 = make_float2(g, g);
+  // thread -> block (r, kb) of the row-major block grid (adjacent threads,
+  // adjacent blocks: coalesced code loads and output stores); the grid
+  // stride is added as (rows, blocks) with one carry, so the loop divides once
+  const uint32_t KB = (uint32_t)(K / 16), nka = (KB + 3) / 4;
+  const uint64_t nblk = (uint64_t)R * KB;
+  const uint64_t b0 = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x, step = (uint64_t)gridDim.x * blockDim.x;
+  if (b0 >= nblk) return;
+  uint64_t r = b0 / KB;
+  uint32_t kb = (uint32_t)(b0 % KB);
+  const uint64_t step_r = step / KB;
+  const uint32_t step_kb = (uint32_t)(step % KB);
+  for (uint64_t b = b0; b < nblk; b += step) {
+    const uint2 c = *reinterpret_cast<const uint2*>(codes + r * (uint64_t)(K / 2) + kb * 8u);
+    const uint32_t s2 = e4m3_f16x2_splat(scales[sf_offset((int64_t)r, kb, nka)] & 0x7Fu);
+    uint32_t h[8];
+    e2m1x16_f16x2(c, h);
+    float2 o[8];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      uint32_t code = ((i < 8 ? c.x : c.y) >> (4 * (i & 7))) & 15u;
-      o[i] = __fmul_rn(__fmul_rn(e2m1_value(code), s), g);
-    }
+    for (int i = 0; i < 8; ++i) o[i] = decode_pair(h[i], s2, g2);
     if constexpr (sizeof(TO) == 4) {
-      float4* d = reinterpret_cast<float4*>(y + r * K + kb * 16);
+      float4* d = reinterpret_cast<float4*>(y + r * (uint64_t)K + kb * 16u);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) d[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+      for (int i = 0; i < 4; ++i) d[i] = make_float4(o[2 * i].x, o[2 * i].y, o[2 * i + 1].x, o[2 * i + 1].y);
     } else {
       uint32_t w[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        __nv_bfloat162 p = __floats2bfloat162_rn(o[2 * i], o[2 * i + 1]);
+        __nv_bfloat162 p = __floats2bfloat162_rn(o[i].x, o[i].y);
         w[i] = *reinterpret_cast<uint32_t*>(&p);
       }
-      uint4* d = reinterpret_cast<uint4*>(y + r * K + kb * 16);
+      uint4* d = reinterpret_cast<uint4*>(y + r * (uint64_t)K + kb * 16u);
       d[0] = make_uint4(w[0], w[1], w[2], w[3]);
       d[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    }
+    kb += step_kb;
+    r += step_r;
+    if (kb >= KB) {
+      kb -= KB;
+      ++r;
     }
   }
 }
@@ -820,7 +839,8 @@ static cudaError_t launch_q(const QuantArgs& a, bool transpose, cudaStream_t s) 
     constexpr int smem = kColRingBytes<T>;
     static OccCache occ = {};
     const unsigned grid = persistent_grid(k, tiles, occ, smem);
-    k<<<grid, 256, smem, s>>>(tm, a);
+    const unsigned long long lim = take_armed_wait(2);  // failure-detection test only
+    k<<<grid, 256, smem, s>>>(tm, a, lim ? 16u : 0u, lim);
   }
   return cudaGetLastError();
 }

@@ -25,38 +25,19 @@
 
 namespace nvfp4 {
 
-// The BF16 weights of one byte of codes (low nibble first), as a bf16x2 word
-// (low half = low nibble): the codes' values scaled by s in f16, exact (every
-// |value * s| lies in [2^-10, 2688], normal f16 with at most 6 significant
-// bits), widened to f32, times g rounded to nearest in f32, then rounded to
-// BF16 (nearest even) -- the dequantization fl(fl(value * s) * g) followed by
-// the BF16 cast.
-__device__ __forceinline__ uint32_t w4a16_pair(uint32_t byte, __half2 s2, float2 g2) {
-  uint32_t h;
-  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(h) : "r"(byte));
-  const float2 vs = __half22float2(__hmul2(*reinterpret_cast<const __half2*>(&h), s2));
-  float2 p;
-  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
-      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
-      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-      : "=f"(p.x), "=f"(p.y)
-      : "f"(vs.x), "f"(vs.y), "f"(g2.x), "f"(g2.y));
-  const __nv_bfloat162 b = __floats2bfloat162_rn(p.x, p.y);
-  return *reinterpret_cast<const uint32_t*>(&b);
-}
-
-// (s, s) in f16 from an E4M3 scale byte (exact: every E4M3 value is an f16).
-__device__ __forceinline__ __half2 e4m3_half2_splat(uint32_t b) {
-  uint32_t h;
-  asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(h) : "r"(b * 0x101u));
-  return *reinterpret_cast<const __half2*>(&h);
-}
-
-// The 16 BF16 weights of one block as 8 bf16x2 words (word p = elements 2p, 2p+1).
+// The 16 BF16 weights of one block as 8 bf16x2 words (word p = elements 2p,
+// 2p+1): the decode fl(fl(value * s) * g) of each pair, rounded to BF16
+// (nearest even).
 __device__ __forceinline__ void w4a16_block(uint2 c, uint32_t sbyte, float2 g2, uint32_t w[8]) {
-  const __half2 s2 = e4m3_half2_splat(sbyte & 0x7Fu);
+  const uint32_t s2 = e4m3_f16x2_splat(sbyte & 0x7Fu);
+  uint32_t h[8];
+  e2m1x16_f16x2(c, h);
 #pragma unroll
-  for (int j = 0; j < 8; ++j) w[j] = w4a16_pair((j < 4 ? c.x : c.y) >> (8 * (j & 3)), s2, g2);
+  for (int j = 0; j < 8; ++j) {
+    const float2 p = decode_pair(h[j], s2, g2);
+    const __nv_bfloat162 b = __floats2bfloat162_rn(p.x, p.y);
+    w[j] = *reinterpret_cast<const uint32_t*>(&b);
+  }
 }
 
 // c += A (16 x 16, BF16, row-major fragment) * B (16 x 8, BF16), FP32.

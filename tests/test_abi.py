@@ -31,7 +31,7 @@ def test_header_declares_the_boundary():
     for required in ["nvfp4_amax", "nvfp4_quantize", "nvfp4_quantize_grouped", "nvfp4_rht_quantize", "nvfp4_dequantize",
                      "nvfp4_transpose_2d", "nvfp4_gemm", "nvfp4_gemm_amax", "nvfp4_gemm_quantize",
                      "nvfp4_gemm_grouped", "nvfp4_w4a16_gemm", "nvfp4_codes_bytes", "nvfp4_scales_bytes", "nvfp4_sync_check",
-                     "nvfp4_status_string", "nvfp4_last_error"]:
+                     "nvfp4_status_string", "nvfp4_last_error", "nvfp4_test_expire_next_wait"]:
         assert required in names
 
 
@@ -212,3 +212,14 @@ def test_gemm_quantize_argument_errors(L):
     assert call(ctypes.byref(A), ctypes.byref(B), amax, ctypes.c_void_p(0x4000008), 256, None, ctypes.byref(out),
                 None) == 3                                                                          # D misaligned
     assert call(ctypes.byref(A), ctypes.byref(B), amax, D, 256, amax, ctypes.byref(out), None) == 1   # aliasing
+
+
+def test_wait_expiry_hook_arguments(L):
+    # no launch happens here: arming only sets a process-wide flag
+    assert L.nvfp4_test_expire_next_wait(0, 20_000_000) == 1
+    assert L.nvfp4_test_expire_next_wait(3, 20_000_000) == 1
+    assert L.nvfp4_test_expire_next_wait(1, 999_999) == 1
+    assert L.nvfp4_test_expire_next_wait(2, 2_000_000_001) == 1
+    for op in (1, 2):
+        assert L.nvfp4_test_expire_next_wait(op, 20_000_000) == 0
+        assert L.nvfp4_test_expire_next_wait(op, 0) == 0  # disarmed again
