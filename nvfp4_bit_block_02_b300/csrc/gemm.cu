@@ -206,6 +206,12 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
                : "memory");
 }
 
+// Bring a tensor map (kernel parameter) into the copy engine's descriptor
+// cache ahead of its first use.
+__device__ __forceinline__ void prefetch_tensor_map(const CUtensorMap* m) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
+}
+
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 // arrive (once, when this thread's MMAs complete) on the barrier at the same
@@ -305,6 +311,7 @@ __device__ __forceinline__ void raster(int t, int mt, int nt, int& pm, int& pn) 
 }
 
 struct SingleSched {
+  static constexpr bool kMapsVary = false;  // one set of tensor maps for every tile
   const CUtensorMap* tmA;
   const CUtensorMap* tmB;
   const CUtensorMap* tmD;
@@ -318,11 +325,16 @@ struct SingleSched {
 };
 
 struct GroupedSched {
+  static constexpr bool kMapsVary = true;  // one set of tensor maps per group
   const GroupedArgs* g;
   __device__ int num_tiles() const { return g->tile_start[g->count]; }
   __device__ Tile get(int t) const {
-    int e = 0;
-    while (e + 1 < g->count && t >= g->tile_start[e + 1]) ++e;
+    int e = 0, hi = g->count - 1;  // the last group whose first tile is <= t (binary search)
+    while (e < hi) {
+      const int mid = (e + hi + 1) >> 1;
+      if (g->tile_start[mid] <= t) e = mid;
+      else hi = mid - 1;
+    }
     Tile x{&g->tmA[e], &g->tmB[e], &g->tmD[e], g->sfa[e], g->sfb[e], g->ga[e], g->gb[e], g->M[e], g->N[e], g->K[e], 0, 0};
     raster(t - g->tile_start[e], (g->M[e] + 2 * BM - 1) / (2 * BM), (g->N[e] + BN - 1) / BN, x.pm, x.pn);
     return x;
@@ -431,6 +443,11 @@ __device__ __forceinline__ void gemm_pairs(const Sched& sched, bool out_bf16, un
       const uint32_t lead_full0 = peer_addr(full0, 0);
       for (int t = first; t < num_tiles && !*abort_flag; t += step) {
         const Tile x = sched.get(t);
+        if (Sched::kMapsVary && t + step < num_tiles) {  // the next tile's maps (another group's)
+          const Tile xn = sched.get(t + step);
+          if (xn.tmA != x.tmA) prefetch_tensor_map(xn.tmA);
+          if (xn.tmB != x.tmB) prefetch_tensor_map(xn.tmB);
+        }
         const int nk = (x.K + 255) / 256;  // the last stage's box is zero-filled past K
         const int m_tile = 2 * x.pm + (int)rank;               // this CTA's 128 A rows
         const bool a_valid = m_tile * BM < x.M;
@@ -594,8 +611,15 @@ __device__ __forceinline__ void gemm_pairs(const Sched& sched, bool out_bf16, un
     const uint32_t stage_u32 = smem_u32(stage);
     const uint32_t lead_accum_empty = peer_addr(accum_empty, 0);
     uint32_t ti = 0;
+    [[maybe_unused]] const CUtensorMap* prev_d = nullptr;
     for (int t = first; t < num_tiles; t += step, ++ti) {
       const Tile x = sched.get(t);
+      if constexpr (Sched::kMapsVary) {
+        if (x.tmD != prev_d) {  // the group's output map, fetched while the mainloop runs
+          if (e == 0 && lane == 0) prefetch_tensor_map(x.tmD);
+          prev_d = x.tmD;
+        }
+      }
       // warp vote: tcgen05.ld is warp-collective
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(accum_full, ti & 1, abort_flag, err, limit))) break;
       tc_fence_after();
