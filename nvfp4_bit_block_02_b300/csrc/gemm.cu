@@ -412,6 +412,13 @@ __device__ __forceinline__ void gemm_pairs(const Sched& sched, bool out_bf16, un
       *qo->amax = amax;
     }
   }
+  if (threadIdx.x == 32 * (NUM_WARPS - 2) && first < num_tiles) {
+    // the first tile's maps start their way into the copy engine during setup
+    const Tile x0 = sched.get(first);
+    prefetch_tensor_map(x0.tmA);
+    prefetch_tensor_map(x0.tmB);
+    if (!QOUT || qo->store_d) prefetch_tensor_map(x0.tmD);  // (a zero map when D is not stored)
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full0 + 8 * s, 1 + 8);

@@ -535,6 +535,7 @@ __device__ __forceinline__ void quant_cols_body(const Src& src, const QuantArgs&
   [[maybe_unused]] const unsigned long long limit = wait_ns ? wait_ns : 2000000000ull;
   if constexpr (TMA) {
     if (t == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
       abort_s = 0;
 #pragma unroll
       for (int i = 0; i < S; ++i) bar_init(&full[i], 1);
