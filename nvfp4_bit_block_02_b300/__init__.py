@@ -146,6 +146,10 @@ class NVFP4Tensor:
                            torch.empty(1, dtype=torch.float32, device=device),
                            torch.empty(1, dtype=torch.float32, device=device), rows, cols)
 
+    def clone(self) -> "NVFP4Tensor":
+        return NVFP4Tensor(self.codes.clone(), self.scales.clone(), self.global_scale.clone(), self.amax.clone(),
+                           self.rows, self.cols)
+
     def c(self) -> CTensor:
         return CTensor(self.codes.data_ptr(), self.scales.data_ptr(), self.global_scale.data_ptr(),
                        self.amax.data_ptr(), self.rows, self.cols)

@@ -48,3 +48,11 @@ def test_oracle_step_pr1_runs_whole_step():
     X, W = bench._oracle_inputs("pr1")
     r = bench._oracle_step("pr1", X, W)
     assert r["step_s"] == r["spent_s"] > 0 and "no extrapolation" in r["work"]
+
+
+def test_operand_copies_exceed_l2():
+    for per_set in (1 << 20, 52 * 2**20, 85 * 2**20, 126 * 2**20 - 1):
+        n = bench.operand_copies(per_set)
+        assert n * per_set > bench.L2_BYTES and (n - 1) * per_set <= bench.L2_BYTES + per_set
+    assert bench.operand_copies(bench.L2_BYTES) == 1
+    assert bench.operand_copies(500 * 2**20) == 1
