@@ -63,3 +63,20 @@ def test_dequantize_llama8b_weight_sampled():
     scales = phys[((r >> 7) * (KB // 4) + (kb >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (kb & 3)]
     yr = oracle.dequantize(codes, scales, float(q.global_scale.cpu()[0]))
     assert torch.equal(y[torch.from_numpy(rows).cuda()].cpu(), torch.from_numpy(yr).to(torch.bfloat16))
+
+
+def test_dequantize_grid_stride_wraps_rows():
+    """More blocks than one pass of the grid (16 CTAs of 256 threads per SM) and
+    a grid stride that is no multiple of the blocks per row (257 here), so every
+    thread's walk carries from row to row at different block columns; the whole
+    output bit-exact with the oracle."""
+    rows, cols = 4800, 4112
+    x = torch.from_numpy(synthetic.normal((rows, cols), 1.0, 52)).to(torch.bfloat16)
+    q = nv.quantize(x.cuda())
+    y32 = nv.dequantize(q, torch.float32)
+    nv.sync_check()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert rows * (cols // 16) > sms * 16 * 256 and (sms * 16 * 256) % (cols // 16) != 0
+    ref = oracle_quantize_like(x.float())
+    yr = oracle.dequantize(ref.codes, ref.scales, ref.g)
+    assert (y32.cpu().numpy().view(np.uint32) == yr.view(np.uint32)).all()
