@@ -298,6 +298,9 @@ struct Tile {
   const float* gb;
   int M, N, K;
   int pm, pn;  // pair-row (256-row) and column (256-col) tile indices
+  int n_tma;   // columns the output map covers (whole 16-byte units of a row)
+  void* d;     // D and its leading dimension, for the columns past n_tma
+  int64_t ldd;
 };
 
 // Raster order: bands of GROUP_M pair rows; inside a band columns advance
@@ -318,7 +321,7 @@ struct SingleSched {
   const GemmArgs* a;
   __device__ int num_tiles() const { return ((a->M + 2 * BM - 1) / (2 * BM)) * ((a->N + BN - 1) / BN); }
   __device__ Tile get(int t) const {
-    Tile x{tmA, tmB, tmD, a->sfa, a->sfb, a->ga, a->gb, a->M, a->N, a->K, 0, 0};
+    Tile x{tmA, tmB, tmD, a->sfa, a->sfb, a->ga, a->gb, a->M, a->N, a->K, 0, 0, a->n_tma, a->d, a->ldd};
     raster(t, (a->M + 2 * BM - 1) / (2 * BM), (a->N + BN - 1) / BN, x.pm, x.pn);
     return x;
   }
@@ -335,7 +338,9 @@ struct GroupedSched {
       if (g->tile_start[mid] <= t) e = mid;
       else hi = mid - 1;
     }
-    Tile x{&g->tmA[e], &g->tmB[e], &g->tmD[e], g->sfa[e], g->sfb[e], g->ga[e], g->gb[e], g->M[e], g->N[e], g->K[e], 0, 0};
+    // (every group's row is a whole number of 16-byte units: ldd = N_e)
+    Tile x{&g->tmA[e], &g->tmB[e], &g->tmD[e], g->sfa[e], g->sfb[e], g->ga[e], g->gb[e], g->M[e], g->N[e], g->K[e], 0, 0,
+           g->N[e], nullptr, 0};
     raster(t - g->tile_start[e], (g->M[e] + 2 * BM - 1) / (2 * BM), (g->N[e] + BN - 1) / BN, x.pm, x.pn);
     return x;
   }
@@ -417,7 +422,8 @@ __device__ __forceinline__ void gemm_pairs(const Sched& sched, bool out_bf16, un
     const Tile x0 = sched.get(first);
     prefetch_tensor_map(x0.tmA);
     prefetch_tensor_map(x0.tmB);
-    if (!QOUT || qo->store_d) prefetch_tensor_map(x0.tmD);  // (a zero map when D is not stored)
+    // (a zero map when D is not stored, or when no row holds a whole 16-byte unit)
+    if ((!QOUT || qo->store_d) && x0.n_tma > 0) prefetch_tensor_map(x0.tmD);
   }
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -639,7 +645,7 @@ __device__ __forceinline__ void gemm_pairs(const Sched& sched, bool out_bf16, un
       const bool active = col0 < x.N && row0 < x.M;
       const int ncols = x.N - col0;           // valid columns of this warp's 128 (may exceed 128)
       const bool row_ok = row0 + lane < x.M;  // this thread's row exists
-      if (out_bf16) {
+      if (QOUT || out_bf16) {  // (the quantizing variant always forms BF16 outputs)
         uint32_t pk[64];
         if (active) {
           // two loads in flight per wait: the accumulator is released after two
@@ -700,9 +706,11 @@ __device__ __forceinline__ void gemm_pairs(const Sched& sched, bool out_bf16, un
           }
         }
         if (active && (!QOUT || qo->store_d)) {
+          // this warp's columns inside whole 16-byte units (all of them when quantizing: N % 16 == 0)
+          const int ntma = QOUT ? ncols : x.n_tma - col0;
 #pragma unroll
           for (int cc = 0; cc < 2; ++cc) {  // 64 columns = one 128-byte box row
-            if (64 * cc >= ncols) break;
+            if (64 * cc >= ntma) break;
             if (lane == 0) bulk_wait_read0();
             __syncwarp();
 #pragma unroll
@@ -715,6 +723,26 @@ __device__ __forceinline__ void gemm_pairs(const Sched& sched, bool out_bf16, un
               tma_store_2d(x.tmD, stage_u32, col0 + 64 * cc, row0);
               bulk_commit();
             }
+          }
+          // (the quantizing variant has N % 16 == 0: whole units only)
+          if (!QOUT && ntma < ncols && ntma < 128 && row_ok) {
+            // the last partial 16-byte unit of the row (1..7 columns from t0,
+            // a multiple of 8): its 4 words picked without dynamic indexing
+            const int t0 = max(ntma, 0), cnt = min(ncols, 128) - t0, gsel = t0 >> 3;
+            uint32_t w4[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+            for (int gi = 0; gi < 16; ++gi)
+              if (gi == gsel) {
+                w4[0] = pk[4 * gi];
+                w4[1] = pk[4 * gi + 1];
+                w4[2] = pk[4 * gi + 2];
+                w4[3] = pk[4 * gi + 3];
+              }
+            unsigned short* dst =
+                reinterpret_cast<unsigned short*>(x.d) + (int64_t)(row0 + lane) * x.ldd + col0 + t0;
+#pragma unroll
+            for (int j = 0; j < 7; ++j)
+              if (j < cnt) dst[j] = (unsigned short)(w4[j >> 1] >> (16 * (j & 1)));
           }
         }
       } else {
@@ -741,7 +769,8 @@ __device__ __forceinline__ void gemm_pairs(const Sched& sched, bool out_bf16, un
             m = __reduce_max_sync(0xFFFFFFFFu, m);
             if (lane == 0 && m) atomicMax(amax_out, m);
           }
-          if (active && 32 * c < ncols) {
+          const int ntma = x.n_tma - col0;
+          if (active && 32 * c < ntma) {
             if (lane == 0) bulk_wait_read0();
             __syncwarp();
 #pragma unroll
@@ -756,6 +785,24 @@ __device__ __forceinline__ void gemm_pairs(const Sched& sched, bool out_bf16, un
               tma_store_2d(x.tmD, stage_u32, col0 + 32 * c, row0);
               bulk_commit();
             }
+          }
+          // the last partial 16-byte unit of the row (1..3 columns from t0, a
+          // multiple of 4), when it lies in this 32-column chunk
+          const int t0 = max(ntma, 0);
+          if (!QOUT && active && row_ok && ntma < ncols && ntma < 128 && (t0 >> 5) == c) {
+            const int cnt = min(ncols, 128) - t0, osel = (t0 & 31) >> 2;
+            float v4[3] = {0.0f, 0.0f, 0.0f};
+#pragma unroll
+            for (int oi = 0; oi < 8; ++oi)
+              if (oi == osel) {
+                v4[0] = __fmul_rn(alpha, __uint_as_float(r[4 * oi]));
+                v4[1] = __fmul_rn(alpha, __uint_as_float(r[4 * oi + 1]));
+                v4[2] = __fmul_rn(alpha, __uint_as_float(r[4 * oi + 2]));
+              }
+            float* dst = reinterpret_cast<float*>(x.d) + (int64_t)(row0 + lane) * x.ldd + col0 + t0;
+#pragma unroll
+            for (int j = 0; j < 3; ++j)
+              if (j < cnt) dst[j] = v4[j];
           }
         }
       }
@@ -989,8 +1036,12 @@ int gemm_tile_n() { return BN; }
 cudaError_t launch_gemm(const GemmOperand& A, const GemmOperand& B, void* D, int64_t ldd, bool out_bf16, cudaStream_t s,
                         const char** why, float* amax_out, const GemmQuantOut* q) {
   CUtensorMap ta, tb, td = {};
+  // the output map covers the whole 16-byte units of each row (TMA clips a
+  // store per 16-byte unit); the kernel writes the remaining columns itself
+  const int es = out_bf16 ? 2 : 4;
+  const int64_t n_tma = (B.rows * es / 16) * 16 / es;
   if (!make_code_map(&ta, A.codes, A.rows, A.K) || !make_code_map(&tb, B.codes, B.rows, B.K) ||
-      (D && !make_out_map(&td, D, A.rows, B.rows, ldd, out_bf16))) {
+      (D && n_tma > 0 && !make_out_map(&td, D, A.rows, n_tma, ldd, out_bf16))) {
     *why = "cuTensorMapEncodeTiled failed (or driver entry point unavailable)";
     return cudaErrorInvalidValue;
   }
@@ -1007,7 +1058,7 @@ cudaError_t launch_gemm(const GemmOperand& A, const GemmOperand& B, void* D, int
     return cudaErrorInvalidValue;
   }
   GemmArgs a{A.scales, B.scales, A.g, B.g, (int)A.rows, (int)B.rows, (int)A.K, out_bf16 ? 1 : 0, err,
-             reinterpret_cast<unsigned int*>(amax_out), q ? *q : GemmQuantOut{}, 0u, 0ull};
+             reinterpret_cast<unsigned int*>(amax_out), q ? *q : GemmQuantOut{}, D, ldd, (int)n_tma, 0u, 0ull};
   if (!q) {
     const unsigned long long lim = take_armed_wait(1);
     if (lim) {  // failure-detection test: 16 bytes that no copy delivers

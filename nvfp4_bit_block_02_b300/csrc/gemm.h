@@ -36,6 +36,12 @@ struct GemmArgs {
   unsigned int* err;
   unsigned int* amax_out;  // nullable: atomicMax of |D| (as stored) over the output, float bits
   GemmQuantOut q;          // used by the quantizing variant only
+  // D for the columns past the last whole 16-byte unit of a row (the output
+  // tensor map covers n_tma = those whole units; its clipping is per 16-byte
+  // unit, so the rest of the row goes through plain stores)
+  void* d;
+  int64_t ldd;
+  int n_tma;
   // Failure-detection test only (0 in every normal launch): extra bytes the
   // leader CTA of each pair expects on its first stage's barrier, which no
   // copy delivers, and the wait limit in ns (0: the default limit).
