@@ -84,3 +84,98 @@ def test_gemm_sweep(i):
     assert_same_quantized(qb, rb, f"B of GEMM case {i}")
     ref, bound = oracle.gemm_reference(ra, rb)
     gemm_check(full[:M, :N], ref, bound, out_dtype == torch.bfloat16, f"GEMM case {i}: {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("i", range(16))
+def test_w4a16_sweep(i):
+    """Random M, N, K (K % 16 == 0) and a padded output row; the padding keeps
+    its canary."""
+    from tests.test_gpu_w4a16 import activations_f32, bf16_activations, random_weight
+    rng = np.random.default_rng(6000 + i)
+    M, N, K = int(rng.integers(1, 41)), int(rng.integers(1, 600)), 16 * int(rng.integers(1, 300))
+    out_dtype = torch.bfloat16 if rng.integers(0, 2) else torch.float32
+    pad = int(rng.integers(0, 10))
+    q, ref = random_weight(N, K, 7000 + i)
+    x = bf16_activations(M, K, 8000 + i)
+    big = torch.full((M + 1, N + pad), -7.0, dtype=out_dtype, device="cuda")
+    nv.w4a16_gemm(x.cuda(), q, out=big[:M, :N])
+    nv.sync_check()
+    full = big.float().cpu().numpy()
+    assert (full[:M, N:] == -7.0).all() and (full[M:] == -7.0).all(), "write outside y"
+    y_ref, bound = oracle.w4a16_reference(activations_f32(x, K), ref)
+    gemm_check(full[:M, :N], y_ref, bound, out_dtype == torch.bfloat16, f"W4A16 case {i}: {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("i", range(8))
+def test_gemm_grouped_sweep(i):
+    """1..6 groups of random shapes (an empty group included at random); each
+    group's rows a whole number of 16-byte units, as the grouped call requires."""
+    rng = np.random.default_rng(9000 + i)
+    out_dtype = torch.bfloat16 if rng.integers(0, 2) else torch.float32
+    per16 = 8 if out_dtype == torch.bfloat16 else 4
+    qa, qb, ra, rb = [], [], [], []
+    for e in range(int(rng.integers(1, 7))):
+        M = 0 if rng.random() < 0.15 else int(rng.integers(1, 300))
+        N = per16 * int(rng.integers(1, 400 // per16))
+        K = 64 * int(rng.integers(1, 9))
+        a = torch.from_numpy(synthetic.normal((max(M, 1), K), 1.0, 9100 + 10 * i + e))[:M]
+        b = torch.from_numpy(synthetic.normal((N, K), 0.05, 9200 + 10 * i + e))
+        qa.append(nv.quantize(a.cuda()) if M else nv.NVFP4Tensor.empty(0, K))
+        qb.append(nv.quantize(b.cuda()))
+        ra.append(oracle_quantize_like(a) if M else None)
+        rb.append(oracle_quantize_like(b))
+    outs = nv.gemm_grouped(qa, qb, out_dtype=out_dtype)
+    nv.sync_check()
+    for e in range(len(qa)):
+        if ra[e] is None:
+            continue
+        assert_same_quantized(qa[e], ra[e], f"A_{e}")
+        ref, bound = oracle.gemm_reference(ra[e], rb[e])
+        gemm_check(outs[e].float().cpu().numpy(), ref, bound, out_dtype == torch.bfloat16, f"grouped case {i} group {e}")
+
+
+@pytest.mark.parametrize("i", range(12))
+def test_gemm_quantize_sweep(i):
+    """Random M, N (N % 16 == 0), K (K % 64 == 0) and tensor amax (exact,
+    loose or saturating): the epilogue encoding equals the oracle's
+    quantization of nvfp4_gemm's BF16 output; the stored D equals it."""
+    rng = np.random.default_rng(10000 + i)
+    M, N, K = int(rng.integers(1, 400)), 16 * int(rng.integers(1, 50)), 64 * int(rng.integers(1, 10))
+    a = torch.from_numpy(synthetic.normal((M, K), 1.0, 10100 + i)).to(torch.bfloat16)
+    b = torch.from_numpy(synthetic.normal((N, K), 0.02, 10200 + i)).to(torch.bfloat16)
+    qa, qb = nv.quantize(a.cuda()), nv.quantize(b.cuda())
+    d_ref, amax_true = nv.gemm_amax(qa, qb, out_dtype=torch.bfloat16)
+    amax_in = amax_true * float(rng.choice([1.0, 3.0, 0.25]))
+    out, bufs = guarded_tensor(M, N)
+    store = bool(rng.integers(0, 2))
+    d = torch.full((M + 1, N + 8), -7.0, dtype=torch.bfloat16, device="cuda")
+    nv.gemm_quantize(qa, qb, amax_in, out=out, d=d[:M, :N] if store else None)
+    nv.sync_check()
+    for buf in bufs:
+        buf.check()
+    if store:
+        assert torch.equal(d[:M, :N], d_ref)
+    assert (d[:M, N:] == -7.0).all() and (d[M:] == -7.0).all(), "write outside D"
+    ref = oracle.quantize(d_ref.float().cpu().numpy(), amax=float(amax_in.cpu()[0]))
+    assert_same_quantized(out, ref, f"gemm_quantize case {i}: {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("i", range(12))
+def test_dequantize_sweep(i):
+    """Random shapes, block modes and scalings; the FP32 output bit-exact with
+    the oracle's decode, the BF16 output its nearest-even rounding."""
+    rng = np.random.default_rng(11000 + i)
+    block = "2d" if rng.integers(0, 2) else "1d"
+    rows, cols = int(rng.integers(1, 500)), 16 * int(rng.integers(1, 80))
+    if block == "2d":
+        rows = 16 * max(1, rows // 16)
+    scaling = "four_over_six" if rng.integers(0, 2) else "max6"
+    x = torch.from_numpy(synthetic.normal((rows, cols), float(10.0 ** rng.uniform(-4, 3)), 11100 + i))
+    q = nv.quantize(x.cuda(), block=block, scaling=scaling)
+    y32 = nv.dequantize(q, torch.float32)
+    y16 = nv.dequantize(q, torch.bfloat16)
+    nv.sync_check()
+    ref = oracle_quantize_like(x, block2d=block == "2d", four_over_six=scaling == "four_over_six")
+    yr = oracle.dequantize(ref.codes, ref.scales, ref.g)
+    assert (y32.cpu().numpy().view(np.uint32) == yr.view(np.uint32)).all()
+    assert torch.equal(y16.cpu(), torch.from_numpy(yr).to(torch.bfloat16))
