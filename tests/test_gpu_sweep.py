@@ -179,3 +179,23 @@ def test_dequantize_sweep(i):
     yr = oracle.dequantize(ref.codes, ref.scales, ref.g)
     assert (y32.cpu().numpy().view(np.uint32) == yr.view(np.uint32)).all()
     assert torch.equal(y16.cpu(), torch.from_numpy(yr).to(torch.bfloat16))
+
+
+@pytest.mark.parametrize("i", range(12))
+def test_rht_sweep(i):
+    """Random RHT configurations (orientation, rounding, scaling, dtype, shape,
+    value scale, wide-span chunks) under the RHT parity rules of
+    tests/test_gpu_rht.py (check_rht)."""
+    from tests.test_gpu_rht import check_rht
+    rng = np.random.default_rng(12000 + i)
+    transpose = bool(rng.integers(0, 2))
+    rounding = "stochastic" if rng.integers(0, 2) else "rne"
+    scaling = "four_over_six" if rng.integers(0, 2) else "max6"
+    dtype = torch.bfloat16 if rng.integers(0, 2) else torch.float32
+    # K = 16 * k along the transform; the transposed input needs its columns % 16
+    rows, cols = 16 * int(rng.integers(1, 30)), 16 * int(rng.integers(1, 30))
+    x = synthetic.student_t((rows, cols), 4, float(10.0 ** rng.uniform(-5, 1)), 12100 + i)
+    if rng.integers(0, 2):  # some chunks with tiny neighbours of large values
+        tiny = rng.random((rows, cols)) < 0.1
+        x[tiny] *= np.exp2(-rng.integers(4, 24, size=int(tiny.sum()))).astype(np.float32)
+    check_rht(torch.from_numpy(x).to(dtype), transpose, rounding, scaling)
