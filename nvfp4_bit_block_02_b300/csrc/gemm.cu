@@ -31,11 +31,16 @@
 //                accumulator half with tcgen05.ld, release it, scale by
 //                g_A*g_B, convert, and write 32 x 128-byte boxes through
 //                swizzled shared memory with TMA stores while the next tile's
-//                mainloop runs.
-// Every mbarrier wait is bounded (kWaitLimitNs).  On expiry the CTA records a
-// timeout in a device word, every role leaves its loop, in-flight copies and
-// MMAs are waited for (bounded), both CTAs meet at a final cluster barrier,
-// tensor memory is freed and the kernel returns.
+//                mainloop runs.  The output map covers the whole 16-byte units
+//                of a row (a TMA store is clipped per 16-byte unit); a row's
+//                last partial unit is written with plain stores.
+// Tensor maps are prefetched into the copy engine's descriptor cache during
+// setup, and (grouped GEMM) the next group's while the current tile runs.
+// Every mbarrier wait is bounded (kWaitLimitNs, or the limit a failure-
+// detection test passes).  On expiry the CTA records a timeout in a device
+// word, every role leaves its loop, in-flight copies and MMAs are waited for
+// (bounded), both CTAs meet at a final cluster barrier, tensor memory is
+// freed and the kernel returns.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>

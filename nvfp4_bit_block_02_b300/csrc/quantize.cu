@@ -7,12 +7,15 @@
 // "Method": 2D 16x16 weight blocks, RHT on Wgrad inputs, SR on gradients);
 // Four-over-Six: the hyper.ai story on the Nemotron 3 Ultra NVFP4 checkpoint.
 //
-// All kernels are HBM-bound.  Each CTA of an encoder owns one 128-row x
-// 4-block tile of the output orientation, i.e. exactly one 512-byte atom of
-// the scale layout, so every scale byte (padding included) is written by the
-// encoder and no memset is needed.  Loads are 16-byte vectors; the transposed
-// encoder stages a 64 x 128 input tile in shared memory and reads it back as
-// column pairs (32-bit words), conflict-free.
+// The kernels are HBM-bound, except the encodes with stochastic rounding plus
+// the RHT and with Four-over-Six, which are bound by ALU issue (Philox draws,
+// the exact transform, two candidate encodes).  Each CTA of an encoder owns
+// one 128-row x 4-block tile of the output orientation, i.e. exactly one
+// 512-byte atom of the scale layout, so every scale byte (padding included)
+// is written by the encoder and no memset is needed.  Loads are 16-byte
+// vectors; the transposed encoder stages a 64 x 128 input tile in shared
+// memory (through a TMA ring for a single tensor) and reads it back as column
+// pairs (32-bit words), conflict-free.
 #include <atomic>
 
 #include "gemm.h"
