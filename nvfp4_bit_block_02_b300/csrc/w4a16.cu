@@ -58,7 +58,7 @@ __device__ __forceinline__ uint2 ld_stream_u2(const uint8_t* p) {
 
 constexpr int kW4Warps = 4;   // warps per CTA, splitting K
 constexpr int kW4Unroll = 2;  // K tiles per warp whose loads are issued together
-constexpr int kW4Acc = 2;     // independent accumulators per token tile (MMA j of a tile -> j % kW4Acc)
+constexpr int kW4AccMax = 2;  // independent accumulators per token tile (MMA j of a tile -> j % kW4Acc)
 
 // NT = token tiles of 8 per pass over the weights (tokens m0 .. m0 + 8 NT - 1).
 template <int NT, bool OUT_BF16>
@@ -67,6 +67,8 @@ __global__ void __launch_bounds__(kW4Warps * 32, 8) k_w4a16(const __nv_bfloat16*
                                                            const uint8_t* __restrict__ scales,
                                                            const float* __restrict__ gptr, int64_t N, int64_t K,
                                                            void* __restrict__ y, int64_t ldy) {
+  // two token tiles already give each warp two independent MMA chains (and one accumulator each avoids spills)
+  constexpr int kW4Acc = NT == 1 ? kW4AccMax : 1;
   __shared__ float part[kW4Warps][NT][8][17];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   const int64_t n0 = (int64_t)blockIdx.x * 16;
