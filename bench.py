@@ -741,34 +741,48 @@ def run_moe(args, rank, world, local_rank):
         se6 += float(((nv.dequantize(q6[e]) - ref) ** 2).double().sum())
     nv.sync_check()
     # end to end: H2D of every expert's W and X from pinned memory, D2H of
-    # every D; the read-back runs on its own stream (the other direction of the
-    # host link) and only the next grouped GEMM, which overwrites D, waits for it
+    # every D, with two device copies of the inputs and of D (as in the other
+    # workloads): step i uploads into set i % 2 on an upload stream once step
+    # i - 2 has quantized from it and reads D back on a download stream; the
+    # grouped GEMM into a set waits only for that set's previous read-back
     d_h = torch.empty((E, M, N), dtype=torch.bfloat16, pin_memory=True)
-    d2h_stream = torch.cuda.Stream(dev)
-    e2e_steps = 2
+    ws2, xs2 = [w, torch.empty_like(w)], [x, torch.empty_like(x)]
+    ds2 = [d, [torch.empty_like(t) for t in d]]
+    up_stream, d2h_stream = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    e2e_steps = 4
+    inputs_free, d_free = [None, None], [None, None]
     torch.cuda.synchronize(dev)
     t0 = time.perf_counter()
-    d_free = None
-    for _ in range(e2e_steps):
+    for i in range(e2e_steps):
+        k = i % 2
         main = torch.cuda.current_stream(dev)
-        w.copy_(w_h, non_blocking=True)
-        x.copy_(x_h, non_blocking=True)
+        with torch.cuda.stream(up_stream):
+            if inputs_free[k] is not None:
+                up_stream.wait_event(inputs_free[k])
+            ws2[k].copy_(w_h, non_blocking=True)
+            xs2[k].copy_(x_h, non_blocking=True)
+            loaded = torch.cuda.Event()
+            loaded.record(up_stream)
+        main.wait_event(loaded)
         fork_stream.wait_stream(main)
-        quant_w()
+        nv.quantize_grouped([ws2[k][e] for e in range(E)], transpose=True, scaling="four_over_six", out=qw)
         with torch.cuda.stream(fork_stream):
-            quant_x()
+            nv.quantize_grouped([xs2[k][e] for e in range(E)], out=qx)
         main.wait_stream(fork_stream)
-        if d_free is not None:
-            main.wait_event(d_free)
-        grouped()
+        inputs_free[k] = torch.cuda.Event()
+        inputs_free[k].record(main)
+        if d_free[k] is not None:
+            main.wait_event(d_free[k])
+        nv.gemm_grouped(qx, qw, out=ds2[k])
         d2h_stream.wait_stream(main)
         with torch.cuda.stream(d2h_stream):
             for e in range(E):
-                d_h[e].copy_(d[e], non_blocking=True)
-            d_free = torch.cuda.Event()
-            d_free.record(d2h_stream)
+                d_h[e].copy_(ds2[k][e], non_blocking=True)
+            d_free[k] = torch.cuda.Event()
+            d_free[k].record(d2h_stream)
     torch.cuda.synchronize(dev)
     e2e_s = (time.perf_counter() - t0) / e2e_steps
+    del ws2, xs2, ds2
     # the roofline's per-launch duration: the grouped GEMM back to back (its
     # operands, 268 MB of codes, exceed L2 on their own)
     g_us = back_to_back_us([lambda: nv.gemm_grouped(qx, qw, out=d)], dev, 6) if rank == 0 else None
