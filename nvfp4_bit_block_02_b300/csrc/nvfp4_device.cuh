@@ -226,11 +226,13 @@ __device__ __forceinline__ float rht_split_const(float m) {
 // Running maximum of |y| over the transformed chunks of a whole warp, exact,
 // for the amax pass (every lane of the warp calls it together; `run_max` and
 // the result are the same in every lane).  A plain fp32 butterfly comes
-// first: each output is within 2^-18 * max|x| <= 2^-18 * max|y| of the exact
-// one (four rounded stages over partial sums bounded by 16 * max|x|, and
-// max|y| >= ||x||_2 since H16 / 4 is orthogonal).  Only when a lane's bound
-// could reach the warp's exact maximum so far are that lane's chunks
-// transformed exactly (rare once the maximum has grown).
+// first: with P = H16 * diag(sigma) * x (so y = P / 4), each of its outputs is
+// within 2^-18 * max|x| of the exact P (four rounded stages over partial sums
+// bounded by 16 * max|x|), and max|P| >= ||P||_2 / 4 = ||x||_2 >= max|x|
+// (H16 * H16^T = 16 I), so the plain maximum m of |P| bounds the exact maximum
+// of |y| by m / 4 * (1 + 2^-17).  Only when a lane's bound could reach the
+// warp's exact maximum so far are that lane's chunks transformed exactly
+// (rare once the maximum has grown).
 __device__ __forceinline__ float rht16x2_absmax(float v[2][16], uint32_t sign_mask, float run_max);
 
 // v[h] <- 1/4 * H16 * diag(sigma) * v[h] for the two 16-element chunks h = 0, 1,
