@@ -1,10 +1,13 @@
 // Device helpers of the NVFP4 kernels (sm_103a).  Every fp32 operation that
 // decides a code or a scale is an explicit IEEE intrinsic (__fmul_rn,
 // __fdiv_rn, __frcp_rn, __fadd_rn, __fsub_rn, and one __fmaf_ru whose exact
-// result is rounded upward on purpose) or a packed PTX multiply with an
-// explicit rounding mode (mul.rn.f32x2) whose result feeds only a conversion,
-// so that the compiler cannot contract or reorder it; the encoder's results
-// are therefore fixed bit for bit by the sequence written in nvfp4.h.
+// result is rounded upward on purpose) or a packed PTX operation with an
+// explicit rounding mode (add/sub/mul/fma .rn.f32x2).  A rounded packed
+// product feeds only a conversion, a store or another packed operation of
+// the correctly rounded transform, where the products are exact (by +-1 or
+// +-1/4); where a rounded product feeds a difference (the Four-over-Six block
+// error) the operations stay scalar.  The encoder's results are therefore
+// fixed bit for bit by the sequence written in nvfp4.h.
 #pragma once
 #include <cstdint>
 #include <cuda_bf16.h>
