@@ -2,10 +2,11 @@
 // decides a code or a scale is an explicit IEEE intrinsic (__fmul_rn,
 // __fdiv_rn, __frcp_rn, __fadd_rn, __fsub_rn, and one __fmaf_ru whose exact
 // result is rounded upward on purpose) or a packed PTX operation with an
-// explicit rounding mode (add/sub/mul/fma .rn.f32x2).  A rounded packed
-// product feeds only a conversion, a store or another packed operation of
-// the correctly rounded transform, where the products are exact (by +-1 or
-// +-1/4); where a rounded product feeds a difference (the Four-over-Six block
+// explicit rounding mode (add/sub/mul/fma .rn.f32x2).  A packed product that
+// rounds is never an operand of a later addition (where it could be fused):
+// it feeds conversions, stores, bit-pattern arithmetic or the multiplicand of
+// an fma; the packed products inside the transform are exact (by +-1 or
+// +-1/4).  Where a rounded product feeds a difference (the Four-over-Six block
 // error) the operations stay scalar.  The encoder's results are therefore
 // fixed bit for bit by the sequence written in nvfp4.h.
 #pragma once
