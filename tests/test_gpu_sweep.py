@@ -199,3 +199,57 @@ def test_rht_sweep(i):
         tiny = rng.random((rows, cols)) < 0.1
         x[tiny] *= np.exp2(-rng.integers(4, 24, size=int(tiny.sum()))).astype(np.float32)
     check_rht(torch.from_numpy(x).to(dtype), transpose, rounding, scaling)
+
+
+@pytest.mark.parametrize("i", range(8))
+def test_quantize_grouped_sweep(i):
+    """1..70 tensors of random shapes in one grouped call (a second launch past
+    64) with a random mode: every group bit-exact with the single-tensor call
+    at offset + e, two groups against the oracle."""
+    rng = np.random.default_rng(13000 + i)
+    block = "2d" if rng.integers(0, 2) else "1d"
+    transpose = bool(rng.integers(0, 2))
+    rounding = "stochastic" if rng.integers(0, 2) else "rne"
+    scaling = "four_over_six" if rng.integers(0, 2) else "max6"
+    dtype = torch.bfloat16 if rng.integers(0, 2) else torch.float32
+    count = int(rng.choice([1, 5, 33, 70]))
+    kw = dict(block=block, rounding=rounding, scaling=scaling, transpose=transpose, seed=int(rng.integers(0, 1000)),
+              offset=int(rng.integers(0, 1000)))
+    xs = []
+    for e in range(count):
+        R, K = int(rng.integers(1, 200)), 16 * int(rng.integers(1, 20))
+        if block == "2d" or transpose:
+            R = 16 * max(1, R // 16)
+        shape = (K, R) if transpose else (R, K)
+        xs.append(torch.from_numpy(synthetic.normal(shape, float(10.0 ** rng.uniform(-3, 2)), 13100 + 100 * i + e))
+                  .to(dtype).cuda())
+    qs = nv.quantize_grouped(xs, **kw)
+    nv.sync_check()
+    for e, x in enumerate(xs):
+        single = nv.quantize(x, **{**kw, "offset": kw["offset"] + e})
+        assert torch.equal(qs[e].codes, single.codes) and torch.equal(qs[e].scales, single.scales), f"group {e}"
+        assert torch.equal(qs[e].amax, single.amax) and torch.equal(qs[e].global_scale, single.global_scale)
+    for e in sorted({0, count - 1}):
+        ref = oracle_quantize_like(xs[e].cpu(), transpose=transpose, block2d=block == "2d",
+                                   stochastic=rounding == "stochastic", four_over_six=scaling == "four_over_six",
+                                   seed=kw["seed"], offset=kw["offset"] + e)
+        assert_same_quantized(qs[e], ref, f"grouped case {i} group {e}")
+
+
+@pytest.mark.parametrize("i", range(8))
+def test_transpose_2d_sweep(i):
+    """Random R x K (both % 16) and scaling, RNE: repacking the 2D quantization
+    of W equals the oracle's 2D quantization of W^T bit for bit."""
+    rng = np.random.default_rng(14000 + i)
+    R, K = 16 * int(rng.integers(1, 60)), 16 * int(rng.integers(1, 60))
+    scaling = "four_over_six" if rng.integers(0, 2) else "max6"
+    dtype = torch.bfloat16 if rng.integers(0, 2) else torch.float32
+    x = torch.from_numpy(synthetic.normal((R, K), float(10.0 ** rng.uniform(-3, 2)), 14100 + i)).to(dtype)
+    q = nv.quantize(x.cuda(), block="2d", scaling=scaling)
+    qt, bufs = guarded_tensor(K, R)
+    nv.transpose_2d(q, out=qt)
+    nv.sync_check()
+    for b in bufs:
+        b.check()
+    ref = oracle_quantize_like(x.t().contiguous(), block2d=True, four_over_six=scaling == "four_over_six")
+    assert_same_quantized(qt, ref, f"transpose_2d case {i}: {R}x{K} {scaling}")
