@@ -12,28 +12,33 @@
 // CTA r of the pair holds rows 128r..128r+127 of the A tile and of the B tile
 // in its shared memory and rows 128r.. of the accumulator in its tensor
 // memory, so each SM loads a quarter of the tile's operand bytes.  Roles in
-// each CTA (15 warps):
+// each CTA (16 warps = 4 warpgroups):
 //   warp 0       TMA producer: its A and B halves (128 B of K = 256 elements
 //                per row, 128B swizzle; completion counted on the leader
 //                CTA's barrier) into a 5-stage ring.
-//   warp 14      scale producer: the stage's scale atoms by cp.async.bulk on a
-//                barrier of their own (issuing them from warp 0 as well slowed
-//                the operand stream by ~15%).
 //   warp 1       tensor memory owner (both CTAs allocate together); in the
 //                leader CTA one thread issues the pair's MMAs and commits to
 //                both CTAs' barriers.
-//   warps 2..5   scale warps: tcgen05.st of the stage's scale bytes into the
+//   warp 2       scale producer: the stage's scale atoms by cp.async.bulk on a
+//                barrier of their own (issuing them from warp 0 as well slowed
+//                the operand stream by ~15%).
+//   warp 3       idle after setup.
+//   warps 4..7   scale warps: tcgen05.st of the stage's scale bytes into the
 //                CTA's tensor memory.  For K-step j the MMA reads the 4 scales
 //                of row r from lane r % 32, column (scale address + r / 32) of
 //                every lane quarter (the layout tcgen05.cp .32x128b.warpx4
 //                makes), scale address = slot + 4j (A), slot + 8j (B).
-//   warps 6..13  epilogue: two warps per lane quarter drain the CTA's 128 x 256
-//                accumulator half with tcgen05.ld, release it, scale by
-//                g_A*g_B, convert, and write 32 x 128-byte boxes through
-//                swizzled shared memory with TMA stores while the next tile's
-//                mainloop runs.  The output map covers the whole 16-byte units
-//                of a row (a TMA store is clipped per 16-byte unit); a row's
-//                last partial unit is written with plain stores.
+//   warps 8..15  epilogue: two warps per lane quarter drain the CTA's 128 x 256
+//                accumulator half with tcgen05.ld (all 128 columns of a warp in
+//                one round trip), release it, scale by g_A*g_B, convert, and
+//                write 32 x 128-byte boxes through swizzled shared memory with
+//                TMA stores while the next tile's mainloop runs.  The output
+//                map covers the whole 16-byte units of a row (a TMA store is
+//                clipped per 16-byte unit); a row's last partial unit is
+//                written with plain stores.
+// The two epilogue warpgroups raise their register limit (setmaxnreg) to hold
+// a warp's 128 accumulator columns at once; the other two lower theirs to
+// pay for it.
 // Tensor maps are prefetched into the copy engine's descriptor cache during
 // setup, and (grouped GEMM) the next group's while the current tile runs.
 // Every mbarrier wait is bounded (kWaitLimitNs, or the limit a failure-
@@ -75,8 +80,18 @@ constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;  // + barriers + alignment slac
 constexpr int TMEM_COLS = 512;
 constexpr int SFA_COL0 = BN;                             // 16 columns per stage
 constexpr int SFB_COL0 = (SFA_COL0 + 16 * STAGES + 31) / 32 * 32;  // 32 columns per stage
-constexpr int NUM_WARPS = 2 + 4 + EPI_WARPS + 1;  // + the scale producer (last warp)
+constexpr int NUM_WARPS = 8 + EPI_WARPS;  // warpgroups 0-1: producers, MMA, scale warps; 2-3: epilogue
 constexpr int NUM_THREADS = 32 * NUM_WARPS;
+// Register split: the kernel is launched with kRegsLaunch per thread; after
+// setup warpgroups 0-1 drop to kRegsLow and the epilogue warpgroups rise to
+// kRegsHigh.  setmaxnreg.inc waits until the registers exist, so the split
+// must add up to exactly what the block was launched with (the host checks
+// the compiled count before the first launch).
+constexpr int kRegsLaunch = 65536 / NUM_THREADS;  // 128
+constexpr int kRegsLow = 88, kRegsHigh = 168;
+static_assert(NUM_WARPS == 16 && EPI_WARPS == 8, "role layout: four whole warpgroups, the last two the epilogue");
+static_assert(2 * 128 * kRegsLow + 2 * 128 * kRegsHigh == NUM_THREADS * kRegsLaunch, "setmaxnreg split");
+static_assert(kRegsLow % 8 == 0 && kRegsHigh % 8 == 0 && kRegsHigh <= 256, "setmaxnreg operands");
 constexpr int GROUP_M = 8;  // raster: bands of 8 pair rows
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 static_assert(SFB_COL0 + 32 * STAGES <= TMEM_COLS, "TMEM budget");
@@ -393,8 +408,10 @@ __device__ __forceinline__ void encode_row_segment(const GemmQuantOut& qo, const
 
 // hold_tx and wait_ns: the failure-detection test's withheld bytes and wait
 // limit (both 0 in normal launches).
-template <class Sched, bool QOUT = false>
-__device__ __forceinline__ void gemm_pairs(const Sched& sched, bool out_bf16, unsigned int* err,
+// OUT_BF16: BF16 output (else FP32); a compile-time choice so that each
+// kernel holds one epilogue.
+template <class Sched, bool QOUT, bool OUT_BF16>
+__device__ __forceinline__ void gemm_pairs(const Sched& sched, unsigned int* err,
                                            unsigned int* amax_out, const GemmQuantOut* qo = nullptr,
                                            uint32_t hold_tx = 0, unsigned long long wait_ns = 0) {
   extern __shared__ uint8_t smem_raw[];
@@ -422,7 +439,7 @@ __device__ __forceinline__ void gemm_pairs(const Sched& sched, bool out_bf16, un
       *qo->amax = amax;
     }
   }
-  if (threadIdx.x == 32 * (NUM_WARPS - 2) && first < num_tiles) {
+  if (threadIdx.x == 32 * 3 && first < num_tiles) {
     // the first tile's maps start their way into the copy engine during setup
     const Tile x0 = sched.get(first);
     prefetch_tensor_map(x0.tmA);
@@ -453,176 +470,181 @@ __device__ __forceinline__ void gemm_pairs(const Sched& sched, bool out_bf16, un
   cluster_sync();  // both CTAs' barriers are initialised before any remote signal
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-
-  if (warp == 0) {
-    // ---------------- TMA producer (each CTA: its halves) ----------------
-    if (lane == 0) {
-      uint32_t it = 0;
-      const uint32_t lead_full0 = peer_addr(full0, 0);
-      for (int t = first; t < num_tiles && !*abort_flag; t += step) {
-        const Tile x = sched.get(t);
-        if (Sched::kMapsVary && t + step < num_tiles) {  // the next tile's maps (another group's)
-          const Tile xn = sched.get(t + step);
-          if (xn.tmA != x.tmA) prefetch_tensor_map(xn.tmA);
-          if (xn.tmB != x.tmB) prefetch_tensor_map(xn.tmB);
+  // the register split: each warpgroup executes one setmaxnreg together, and
+  // only the epilogue code follows the increase
+  if (warp < 8) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
+    if (warp == 0) {
+      // ---------------- TMA producer (each CTA: its halves) ----------------
+      if (lane == 0) {
+        uint32_t it = 0;
+        const uint32_t lead_full0 = peer_addr(full0, 0);
+        for (int t = first; t < num_tiles && !*abort_flag; t += step) {
+          const Tile x = sched.get(t);
+          if (Sched::kMapsVary && t + step < num_tiles) {  // the next tile's maps (another group's)
+            const Tile xn = sched.get(t + step);
+            if (xn.tmA != x.tmA) prefetch_tensor_map(xn.tmA);
+            if (xn.tmB != x.tmB) prefetch_tensor_map(xn.tmB);
+          }
+          const int nk = (x.K + 255) / 256;  // the last stage's box is zero-filled past K
+          const int m_tile = 2 * x.pm + (int)rank;               // this CTA's 128 A rows
+          const bool a_valid = m_tile * BM < x.M;
+          const int nb_mine = 2 * x.pn + (int)rank;              // this CTA's 128 B rows
+          const bool b_valid = nb_mine * 128 < x.N;
+          // the leader's halves always exist; the peer's may not (M or N % 256 == 128)
+          const uint32_t ab_tx = A_BYTES * (1 + ((2 * x.pm + 1) * BM < x.M)) + B_BYTES * (1 + ((2 * x.pn + 1) * 128 < x.N));
+          for (int kt = 0; kt < nk; ++kt, ++it) {
+            const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
+            if (!mbar_wait(empty0 + 8 * s, ph ^ 1, abort_flag, err, limit)) break;
+            // A/B: the leader expects both CTAs' bytes on its own barrier
+            if (leader) mbar_expect_tx(full0 + 8 * s, ab_tx + (it == 0 ? hold_tx : 0u));
+            const uint32_t fb = lead_full0 + 8 * s;
+            if (a_valid) tma_load_pair(smem_u32(smem + OFF_A + s * A_BYTES), x.tmA, kt * BKB, m_tile * BM, fb);
+            if (b_valid) tma_load_pair(smem_u32(smem + OFF_B + s * B_BYTES), x.tmB, kt * BKB, nb_mine * 128, fb);
+          }
         }
-        const int nk = (x.K + 255) / 256;  // the last stage's box is zero-filled past K
-        const int m_tile = 2 * x.pm + (int)rank;               // this CTA's 128 A rows
-        const bool a_valid = m_tile * BM < x.M;
-        const int nb_mine = 2 * x.pn + (int)rank;              // this CTA's 128 B rows
-        const bool b_valid = nb_mine * 128 < x.N;
-        // the leader's halves always exist; the peer's may not (M or N % 256 == 128)
-        const uint32_t ab_tx = A_BYTES * (1 + ((2 * x.pm + 1) * BM < x.M)) + B_BYTES * (1 + ((2 * x.pn + 1) * 128 < x.N));
-        for (int kt = 0; kt < nk; ++kt, ++it) {
-          const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
-          if (!mbar_wait(empty0 + 8 * s, ph ^ 1, abort_flag, err, limit)) break;
-          // A/B: the leader expects both CTAs' bytes on its own barrier
-          if (leader) mbar_expect_tx(full0 + 8 * s, ab_tx + (it == 0 ? hold_tx : 0u));
-          const uint32_t fb = lead_full0 + 8 * s;
-          if (a_valid) tma_load_pair(smem_u32(smem + OFF_A + s * A_BYTES), x.tmA, kt * BKB, m_tile * BM, fb);
-          if (b_valid) tma_load_pair(smem_u32(smem + OFF_B + s * B_BYTES), x.tmB, kt * BKB, nb_mine * 128, fb);
-        }
-      }
-      if (*abort_flag) {
-        // Copies already issued must land before the pair leaves.  They
-        // complete on the leader's full barriers, which the leader drains
-        // (bounded: a phase whose scale-warp arrivals were abandoned never
-        // completes); the peer cannot observe them and waits 2 ms instead.
-        if (leader) {
-          for (uint32_t i = it > STAGES ? it - STAGES : 0; i < it; ++i)
-            mbar_drain(full0 + 8 * (i % STAGES), (i / STAGES) & 1);
-        } else {
-          const unsigned long long t0 = now_ns();
-          while (now_ns() - t0 < 2000000ull) {
+        if (*abort_flag) {
+          // Copies already issued must land before the pair leaves.  They
+          // complete on the leader's full barriers, which the leader drains
+          // (bounded: a phase whose scale-warp arrivals were abandoned never
+          // completes); the peer cannot observe them and waits 2 ms instead.
+          if (leader) {
+            for (uint32_t i = it > STAGES ? it - STAGES : 0; i < it; ++i)
+              mbar_drain(full0 + 8 * (i % STAGES), (i / STAGES) & 1);
+          } else {
+            const unsigned long long t0 = now_ns();
+            while (now_ns() - t0 < 2000000ull) {
+            }
           }
         }
       }
-    }
-  } else if (warp == 1) {
-    // ---------------- MMA issuer (leader CTA) ----------------
-    if (leader && lane == 0) {
-      // the MMA issue queue is shallow, so every cycle spent between stages
-      // idles the tensor pipe: one barrier poll per stage, stage and phase kept
-      // incrementally, descriptors advanced by adding to their address field
-      // (K-step j is 32 bytes = 2 units further; a stage is A_BYTES / 16 units)
-      // The next stage's barrier is tested between the MMAs of the current
-      // one, while the tensor pipe is busy, so a ready stage costs no poll.
-      const uint64_t da0 = desc_sw128(smem_u32(smem + OFF_A)), db0 = desc_sw128(smem_u32(smem + OFF_B));
-      uint32_t s = 0, ph = 0, ti = 0;
-      bool ok = true, next_ready = false;
-      for (int t = first; t < num_tiles && ok; t += step, ++ti) {
+    } else if (warp == 1) {
+      // ---------------- MMA issuer (leader CTA) ----------------
+      if (leader && lane == 0) {
+        // the MMA issue queue is shallow, so every cycle spent between stages
+        // idles the tensor pipe: one barrier poll per stage, stage and phase kept
+        // incrementally, descriptors advanced by adding to their address field
+        // (K-step j is 32 bytes = 2 units further; a stage is A_BYTES / 16 units)
+        // The next stage's barrier is tested between the MMAs of the current
+        // one, while the tensor pipe is busy, so a ready stage costs no poll.
+        const uint64_t da0 = desc_sw128(smem_u32(smem + OFF_A)), db0 = desc_sw128(smem_u32(smem + OFF_B));
+        uint32_t s = 0, ph = 0, ti = 0;
+        bool ok = true, next_ready = false;
+        for (int t = first; t < num_tiles && ok; t += step, ++ti) {
+          const Tile x = sched.get(t);
+          const int nk = (x.K + 255) / 256, nkc = x.K / 64;
+          if (!mbar_wait(accum_empty, (ti & 1) ^ 1, abort_flag, err, limit)) break;
+          tc_fence_after();
+          for (int kt = 0; kt < nk; ++kt) {
+            if (!next_ready && !mbar_wait(full0 + 8 * s, ph, abort_flag, err, limit)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t sn = s + 1 == STAGES ? 0 : s + 1, phn = s + 1 == STAGES ? ph ^ 1 : ph;
+            const uint64_t da = da0 + (uint64_t)(s * (A_BYTES >> 4)), db = db0 + (uint64_t)(s * (B_BYTES >> 4));
+            const uint32_t sfa = tmem + SFA_COL0 + 16 * s, sfb = tmem + SFB_COL0 + 32 * s;
+            const int kc = nkc - 4 * kt;  // K-steps of 64 left: 4 or more except in a K-tail stage
+            if (kc >= 4) {
+  #pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                tc_mma_pair(tmem, da + 2 * j, db + 2 * j, sfa + 4 * j, sfb + 8 * j, (kt | j) != 0);
+                if (j == 2) next_ready = mbar_test(full0 + 8 * sn, phn);
+              }
+            } else {
+  #pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                if (j < kc) tc_mma_pair(tmem, da + 2 * j, db + 2 * j, sfa + 4 * j, sfb + 8 * j, (kt | j) != 0);
+                if (j == 2) next_ready = mbar_test(full0 + 8 * sn, phn);
+              }
+            }
+            tc_commit_pair(empty0 + 8 * s);
+            s = sn;
+            ph = phn;
+          }
+          next_ready = next_ready && ok;
+          if (ok) tc_commit_pair(accum_full);
+        }
+        tc_commit_pair(drain);  // arrives when every MMA this thread issued has completed
+        mbar_drain(drain, 0);
+      }
+    } else if (warp >= 4) {
+      // ---------------- scale warps: shared memory -> TMEM ----------------
+      const uint32_t q = warp & 3;
+      const uint32_t lane_base = (q * 32) << 16;
+      const uint32_t lead_full0 = peer_addr(full0, 0);
+      uint32_t it = 0;
+      bool ok = true;
+      for (int t = first; t < num_tiles && ok; t += step) {
         const Tile x = sched.get(t);
-        const int nk = (x.K + 255) / 256, nkc = x.K / 64;
-        if (!mbar_wait(accum_empty, (ti & 1) ^ 1, abort_flag, err, limit)) break;
-        tc_fence_after();
-        for (int kt = 0; kt < nk; ++kt) {
-          if (!next_ready && !mbar_wait(full0 + 8 * s, ph, abort_flag, err, limit)) {
+        const int nk = (x.K + 255) / 256;
+        for (int kt = 0; kt < nk; ++kt, ++it) {
+          const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
+          // warp vote: the tcgen05.st below is warp-collective
+          if (!__all_sync(0xFFFFFFFFu, mbar_wait(sff0 + 8 * s, ph, abort_flag, err, limit))) {
             ok = false;
             break;
           }
-          tc_fence_after();
-          const uint32_t sn = s + 1 == STAGES ? 0 : s + 1, phn = s + 1 == STAGES ? ph ^ 1 : ph;
-          const uint64_t da = da0 + (uint64_t)(s * (A_BYTES >> 4)), db = db0 + (uint64_t)(s * (B_BYTES >> 4));
-          const uint32_t sfa = tmem + SFA_COL0 + 16 * s, sfb = tmem + SFB_COL0 + 32 * s;
-          const int kc = nkc - 4 * kt;  // K-steps of 64 left: 4 or more except in a K-tail stage
-          if (kc >= 4) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              tc_mma_pair(tmem, da + 2 * j, db + 2 * j, sfa + 4 * j, sfb + 8 * j, (kt | j) != 0);
-              if (j == 2) next_ready = mbar_test(full0 + 8 * sn, phn);
-            }
-          } else {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              if (j < kc) tc_mma_pair(tmem, da + 2 * j, db + 2 * j, sfa + 4 * j, sfb + 8 * j, (kt | j) != 0);
-              if (j == 2) next_ready = mbar_test(full0 + 8 * sn, phn);
-            }
+          // lane l: row l of every 512-byte atom = 16 bytes = 4 consecutive columns
+          const uint4* sa = reinterpret_cast<const uint4*>(smem + OFF_SFA + s * SFA_BYTES) + lane;
+          const uint4* sb = reinterpret_cast<const uint4*>(smem + OFF_SFB + s * SFB_BYTES) + lane;
+          uint32_t va[16], vb[32];
+  #pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint4 wa = sa[j * 32];
+            va[4 * j] = wa.x; va[4 * j + 1] = wa.y; va[4 * j + 2] = wa.z; va[4 * j + 3] = wa.w;
+            const uint4 w0 = sb[j * 32];        // B rows 0..127 of the tile
+            const uint4 w1 = sb[128 + j * 32];  // B rows 128..255
+            vb[8 * j] = w0.x; vb[8 * j + 1] = w0.y; vb[8 * j + 2] = w0.z; vb[8 * j + 3] = w0.w;
+            vb[8 * j + 4] = w1.x; vb[8 * j + 5] = w1.y; vb[8 * j + 6] = w1.z; vb[8 * j + 7] = w1.w;
           }
-          tc_commit_pair(empty0 + 8 * s);
-          s = sn;
-          ph = phn;
-        }
-        next_ready = next_ready && ok;
-        if (ok) tc_commit_pair(accum_full);
-      }
-      tc_commit_pair(drain);  // arrives when every MMA this thread issued has completed
-      mbar_drain(drain, 0);
-    }
-  } else if (warp < 6) {
-    // ---------------- scale warps: shared memory -> TMEM ----------------
-    const uint32_t q = warp & 3;
-    const uint32_t lane_base = (q * 32) << 16;
-    const uint32_t lead_full0 = peer_addr(full0, 0);
-    uint32_t it = 0;
-    bool ok = true;
-    for (int t = first; t < num_tiles && ok; t += step) {
-      const Tile x = sched.get(t);
-      const int nk = (x.K + 255) / 256;
-      for (int kt = 0; kt < nk; ++kt, ++it) {
-        const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
-        // warp vote: the tcgen05.st below is warp-collective
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(sff0 + 8 * s, ph, abort_flag, err, limit))) {
-          ok = false;
-          break;
-        }
-        // lane l: row l of every 512-byte atom = 16 bytes = 4 consecutive columns
-        const uint4* sa = reinterpret_cast<const uint4*>(smem + OFF_SFA + s * SFA_BYTES) + lane;
-        const uint4* sb = reinterpret_cast<const uint4*>(smem + OFF_SFB + s * SFB_BYTES) + lane;
-        uint32_t va[16], vb[32];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint4 wa = sa[j * 32];
-          va[4 * j] = wa.x; va[4 * j + 1] = wa.y; va[4 * j + 2] = wa.z; va[4 * j + 3] = wa.w;
-          const uint4 w0 = sb[j * 32];        // B rows 0..127 of the tile
-          const uint4 w1 = sb[128 + j * 32];  // B rows 128..255
-          vb[8 * j] = w0.x; vb[8 * j + 1] = w0.y; vb[8 * j + 2] = w0.z; vb[8 * j + 3] = w0.w;
-          vb[8 * j + 4] = w1.x; vb[8 * j + 5] = w1.y; vb[8 * j + 6] = w1.z; vb[8 * j + 7] = w1.w;
-        }
-        tmem_st16(tmem + lane_base + SFA_COL0 + 16 * s, va);
-        tmem_st32(tmem + lane_base + SFB_COL0 + 32 * s, vb);
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(lead_full0 + 8 * s);
-      }
-    }
-  } else if (warp == NUM_WARPS - 1) {
-    // ---------------- scale producer (each CTA: its scale atoms) ----------------
-    if (lane == 0) {
-      uint32_t it = 0;
-      for (int t = first; t < num_tiles && !*abort_flag; t += step) {
-        const Tile x = sched.get(t);
-        const int nk = (x.K + 255) / 256;
-        const int nka = x.K / 64;  // 4-block scale atoms per 128 rows (K % 64 == 0)
-        const int m_tile = 2 * x.pm + (int)rank;
-        const bool a_valid = m_tile * BM < x.M;
-        // 128-row scale blocks of B that exist (the buffer is padded to 128 rows)
-        const int sfb_blocks = min(2, (x.N - x.pn * BN + 127) / 128);
-        const int sfb_first = 2 * x.pn;
-        for (int kt = 0; kt < nk; ++kt, ++it) {
-          const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
-          if (!mbar_wait(empty0 + 8 * s, ph ^ 1, abort_flag, err, limit)) break;
-          // the atoms of this stage's K-steps: 4, or fewer at a K tail (the
-          // next atoms in memory belong to the next 128 rows)
-          const uint32_t bytes = (uint32_t)min(4, nka - 4 * kt) * 512;
-          const uint32_t sb = sff0 + 8 * s;
-          mbar_expect_tx(sb, (a_valid ? bytes : 0) + sfb_blocks * bytes);
-          if (a_valid)
-            bulk_g2s(smem_u32(smem + OFF_SFA + s * SFA_BYTES), x.sfa + ((int64_t)m_tile * nka + 4 * kt) * 512,
-                     bytes, sb);
-          for (int nb = 0; nb < sfb_blocks; ++nb)
-            bulk_g2s(smem_u32(smem + OFF_SFB + s * SFB_BYTES + nb * 2048),
-                     x.sfb + ((int64_t)(sfb_first + nb) * nka + 4 * kt) * 512, bytes, sb);
+          tmem_st16(tmem + lane_base + SFA_COL0 + 16 * s, va);
+          tmem_st32(tmem + lane_base + SFB_COL0 + 32 * s, vb);
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(lead_full0 + 8 * s);
         }
       }
-      // copies already issued land on this CTA's own scale barriers: drain
-      // the last round of every slot before the CTA leaves
-      if (*abort_flag)
-        for (uint32_t i = it > STAGES ? it - STAGES : 0; i < it; ++i) mbar_drain(sff0 + 8 * (i % STAGES), (i / STAGES) & 1);
+    } else if (warp == 2) {
+      // ---------------- scale producer (each CTA: its scale atoms) ----------------
+      if (lane == 0) {
+        uint32_t it = 0;
+        for (int t = first; t < num_tiles && !*abort_flag; t += step) {
+          const Tile x = sched.get(t);
+          const int nk = (x.K + 255) / 256;
+          const int nka = x.K / 64;  // 4-block scale atoms per 128 rows (K % 64 == 0)
+          const int m_tile = 2 * x.pm + (int)rank;
+          const bool a_valid = m_tile * BM < x.M;
+          // 128-row scale blocks of B that exist (the buffer is padded to 128 rows)
+          const int sfb_blocks = min(2, (x.N - x.pn * BN + 127) / 128);
+          const int sfb_first = 2 * x.pn;
+          for (int kt = 0; kt < nk; ++kt, ++it) {
+            const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
+            if (!mbar_wait(empty0 + 8 * s, ph ^ 1, abort_flag, err, limit)) break;
+            // the atoms of this stage's K-steps: 4, or fewer at a K tail (the
+            // next atoms in memory belong to the next 128 rows)
+            const uint32_t bytes = (uint32_t)min(4, nka - 4 * kt) * 512;
+            const uint32_t sb = sff0 + 8 * s;
+            mbar_expect_tx(sb, (a_valid ? bytes : 0) + sfb_blocks * bytes);
+            if (a_valid)
+              bulk_g2s(smem_u32(smem + OFF_SFA + s * SFA_BYTES), x.sfa + ((int64_t)m_tile * nka + 4 * kt) * 512,
+                       bytes, sb);
+            for (int nb = 0; nb < sfb_blocks; ++nb)
+              bulk_g2s(smem_u32(smem + OFF_SFB + s * SFB_BYTES + nb * 2048),
+                       x.sfb + ((int64_t)(sfb_first + nb) * nka + 4 * kt) * 512, bytes, sb);
+          }
+        }
+        // copies already issued land on this CTA's own scale barriers: drain
+        // the last round of every slot before the CTA leaves
+        if (*abort_flag)
+          for (uint32_t i = it > STAGES ? it - STAGES : 0; i < it; ++i) mbar_drain(sff0 + 8 * (i % STAGES), (i / STAGES) & 1);
+      }
     }
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
     // ---------------- epilogue (each CTA: its 128 accumulator rows) ----------------
-    const int e = warp - 6;
+    const int e = warp - 8;
     const uint32_t q = warp & 3, half = e >> 2;
     const uint32_t taddr0 = tmem + ((q * 32) << 16) + half * 128;
     uint8_t* stage = smem + OFF_EPI + e * EPI_BYTES;
@@ -650,31 +672,33 @@ __device__ __forceinline__ void gemm_pairs(const Sched& sched, bool out_bf16, un
       const bool active = col0 < x.N && row0 < x.M;
       const int ncols = x.N - col0;           // valid columns of this warp's 128 (may exceed 128)
       const bool row_ok = row0 + lane < x.M;  // this thread's row exists
-      if (QOUT || out_bf16) {  // (the quantizing variant always forms BF16 outputs)
+      if constexpr (QOUT || OUT_BF16) {  // (the quantizing variant always forms BF16 outputs)
         uint32_t pk[64];
         if (active) {
-          // two loads in flight per wait: the accumulator is released after two
-          // TMEM round trips instead of four
+          // the warp's 128 columns in one round trip; the accumulator is
+          // released as soon as they are in registers, before converting
+          uint32_t r0[32], r1[32], r2[32], r3[32];
+          NVFP4_LD32(taddr0, r0);
+          NVFP4_LD32(taddr0 + 32, r1);
+          NVFP4_LD32(taddr0 + 64, r2);
+          NVFP4_LD32(taddr0 + 96, r3);
+          tmem_ld_wait();
+          NVFP4_LD_FENCE(r0);
+          NVFP4_LD_FENCE(r1);
+          NVFP4_LD_FENCE(r2);
+          NVFP4_LD_FENCE(r3);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(lead_accum_empty);
 #pragma unroll
-          for (int c = 0; c < 4; c += 2) {
-            uint32_t r0[32], r1[32];
-            NVFP4_LD32(taddr0 + c * 32, r0);
-            NVFP4_LD32(taddr0 + c * 32 + 32, r1);
-            tmem_ld_wait();
-            NVFP4_LD_FENCE(r0);
-            NVFP4_LD_FENCE(r1);
-            if (c == 2) {  // every column is in registers: release the accumulator before converting
-              tc_fence_before();
-              __syncwarp();
-              if (lane == 0) mbar_arrive_cluster(lead_accum_empty);
-            }
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              pk[16 * c + i] = pack_bf16(__fmul_rn(alpha, __uint_as_float(r0[2 * i])),
-                                         __fmul_rn(alpha, __uint_as_float(r0[2 * i + 1])));
-              pk[16 * c + 16 + i] = pack_bf16(__fmul_rn(alpha, __uint_as_float(r1[2 * i])),
-                                              __fmul_rn(alpha, __uint_as_float(r1[2 * i + 1])));
-            }
+          for (int i = 0; i < 16; ++i) {
+            pk[i] = pack_bf16(__fmul_rn(alpha, __uint_as_float(r0[2 * i])), __fmul_rn(alpha, __uint_as_float(r0[2 * i + 1])));
+            pk[16 + i] =
+                pack_bf16(__fmul_rn(alpha, __uint_as_float(r1[2 * i])), __fmul_rn(alpha, __uint_as_float(r1[2 * i + 1])));
+            pk[32 + i] =
+                pack_bf16(__fmul_rn(alpha, __uint_as_float(r2[2 * i])), __fmul_rn(alpha, __uint_as_float(r2[2 * i + 1])));
+            pk[48 + i] =
+                pack_bf16(__fmul_rn(alpha, __uint_as_float(r3[2 * i])), __fmul_rn(alpha, __uint_as_float(r3[2 * i + 1])));
           }
         }
         if (!active) {  // nothing was loaded: release right away
@@ -751,39 +775,45 @@ __device__ __forceinline__ void gemm_pairs(const Sched& sched, bool out_bf16, un
           }
         }
       } else {
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t r[32];
-          if (active) {
-            NVFP4_LD32(taddr0 + c * 32, r);
-            tmem_ld_wait();
-            NVFP4_LD_FENCE(r);
-          }
-          if (c == 3) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(lead_accum_empty);
-          }
+        // the warp's 128 columns in one round trip, then the accumulator is
+        // released before the four 32-column boxes are staged and stored
+        uint32_t r0[32], r1[32], r2[32], r3[32];
+        if (active) {
+          NVFP4_LD32(taddr0, r0);
+          NVFP4_LD32(taddr0 + 32, r1);
+          NVFP4_LD32(taddr0 + 64, r2);
+          NVFP4_LD32(taddr0 + 96, r3);
+          tmem_ld_wait();
+          NVFP4_LD_FENCE(r0);
+          NVFP4_LD_FENCE(r1);
+          NVFP4_LD_FENCE(r2);
+          NVFP4_LD_FENCE(r3);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(lead_accum_empty);
+        const int ntma = x.n_tma - col0;
+        // one 32-column chunk: scaled in place (one product per output), then
+        // the producer amax, the TMA box and the row's partial last unit
+        auto chunk = [&](uint32_t (&r)[32], const int c) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__fmul_rn(alpha, __uint_as_float(r[i])));
           if (amax_out && active) {
             uint32_t m = 0;
 #pragma unroll
             for (int i = 0; i < 32; ++i)
-              if (32 * c + i < ncols)
-                m = max(m, __float_as_uint(__fmul_rn(alpha, __uint_as_float(r[i]))) & 0x7FFFFFFFu);
+              if (32 * c + i < ncols) m = max(m, r[i] & 0x7FFFFFFFu);
             if (!row_ok) m = 0;
             m = __reduce_max_sync(0xFFFFFFFFu, m);
             if (lane == 0 && m) atomicMax(amax_out, m);
           }
-          const int ntma = x.n_tma - col0;
           if (active && 32 * c < ntma) {
             if (lane == 0) bulk_wait_read0();
             __syncwarp();
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-              *reinterpret_cast<float4*>(stage + lane * 128 + ((i ^ (lane & 7)) << 4)) =
-                  make_float4(__fmul_rn(alpha, __uint_as_float(r[4 * i])), __fmul_rn(alpha, __uint_as_float(r[4 * i + 1])),
-                              __fmul_rn(alpha, __uint_as_float(r[4 * i + 2])),
-                              __fmul_rn(alpha, __uint_as_float(r[4 * i + 3])));
+              *reinterpret_cast<uint4*>(stage + lane * 128 + ((i ^ (lane & 7)) << 4)) =
+                  make_uint4(r[4 * i], r[4 * i + 1], r[4 * i + 2], r[4 * i + 3]);
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
             if (lane == 0) {
@@ -796,20 +826,24 @@ __device__ __forceinline__ void gemm_pairs(const Sched& sched, bool out_bf16, un
           const int t0 = max(ntma, 0);
           if (!QOUT && active && row_ok && ntma < ncols && ntma < 128 && (t0 >> 5) == c) {
             const int cnt = min(ncols, 128) - t0, osel = (t0 & 31) >> 2;
-            float v4[3] = {0.0f, 0.0f, 0.0f};
+            uint32_t v4[3] = {0u, 0u, 0u};
 #pragma unroll
             for (int oi = 0; oi < 8; ++oi)
               if (oi == osel) {
-                v4[0] = __fmul_rn(alpha, __uint_as_float(r[4 * oi]));
-                v4[1] = __fmul_rn(alpha, __uint_as_float(r[4 * oi + 1]));
-                v4[2] = __fmul_rn(alpha, __uint_as_float(r[4 * oi + 2]));
+                v4[0] = r[4 * oi];
+                v4[1] = r[4 * oi + 1];
+                v4[2] = r[4 * oi + 2];
               }
-            float* dst = reinterpret_cast<float*>(x.d) + (int64_t)(row0 + lane) * x.ldd + col0 + t0;
+            uint32_t* dst = reinterpret_cast<uint32_t*>(x.d) + (int64_t)(row0 + lane) * x.ldd + col0 + t0;
 #pragma unroll
             for (int j = 0; j < 3; ++j)
               if (j < cnt) dst[j] = v4[j];
           }
-        }
+        };
+        chunk(r0, 0);
+        chunk(r1, 1);
+        chunk(r2, 2);
+        chunk(r3, 3);
       }
     }
     if (lane == 0) bulk_wait0();
@@ -825,11 +859,12 @@ __device__ __forceinline__ void gemm_pairs(const Sched& sched, bool out_bf16, un
   }
 }
 
+template <bool OUT_BF16>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
            const __grid_constant__ CUtensorMap tmD, const __grid_constant__ GemmArgs a) {
   SingleSched s{&tmA, &tmB, &tmD, &a};
-  gemm_pairs(s, a.out_bf16 != 0, a.err, a.amax_out, nullptr, a.hold_tx, a.wait_ns);
+  gemm_pairs<SingleSched, false, OUT_BF16>(s, a.err, a.amax_out, nullptr, a.hold_tx, a.wait_ns);
 }
 
 // The GEMM with the NVFP4 encoding of its BF16 output in the epilogue.
@@ -837,12 +872,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_gemm_quant(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const __grid_constant__ CUtensorMap tmD, const __grid_constant__ GemmArgs a) {
   SingleSched s{&tmA, &tmB, &tmD, &a};
-  gemm_pairs<SingleSched, true>(s, true, a.err, a.amax_out, &a.q);
+  gemm_pairs<SingleSched, true, true>(s, a.err, a.amax_out, &a.q);
 }
 
+template <bool OUT_BF16>
 __global__ void __launch_bounds__(NUM_THREADS, 1) k_gemm_grouped(const __grid_constant__ GroupedArgs g) {
   GroupedSched s{&g};
-  gemm_pairs(s, g.out_bf16 != 0, g.err, nullptr);
+  gemm_pairs<GroupedSched, false, OUT_BF16>(s, g.err, nullptr);
 }
 
 // ---------------------------------------------------------------------------
@@ -909,7 +945,7 @@ bool make_out_map(CUtensorMap* m, void* d, int64_t rows, int64_t cols, int64_t l
 // concurrent first calls compute the same values, and the atomics make the
 // publication safe.
 constexpr int kMaxDevices = 64;
-enum KernelId { kSingle = 0, kGrouped = 1, kSingleQuant = 2, kNumKernels = 3 };
+enum KernelId { kSingleF32 = 0, kSingleBf16, kSingleQuant, kGroupedF32, kGroupedBf16, kNumKernels };
 struct DeviceState {
   std::atomic<unsigned int*> err{nullptr};
   std::atomic<unsigned int*> err_taken{nullptr};
@@ -941,9 +977,21 @@ int num_sms(DeviceState* st) {
   return n;
 }
 
-bool smem_configured(DeviceState* st, KernelId k, const void* fn) {
+// The shared-memory opt-in, and the check that the kernel was compiled to
+// kRegsLaunch registers per thread: the setmaxnreg split inside it adds up to
+// exactly that many, and with fewer the epilogue's increase would wait for
+// registers that never come.
+bool kernel_configured(DeviceState* st, KernelId k, const void* fn, const char** why) {
   if (st->smem_ok[k].load(std::memory_order_acquire)) return true;
-  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess) return false;
+  cudaFuncAttributes fa;
+  if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess || fa.numRegs != kRegsLaunch) {
+    *why = "GEMM kernel not compiled to the register count its setmaxnreg split assumes";
+    return false;
+  }
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess) {
+    *why = "cudaFuncSetAttribute failed";
+    return false;
+  }
   st->smem_ok[k].store(true, std::memory_order_release);
   return true;
 }
@@ -1056,13 +1104,10 @@ cudaError_t launch_gemm(const GemmOperand& A, const GemmOperand& B, void* D, int
     *why = "device error word unavailable";
     return cudaErrorInvalidValue;
   }
-  const KernelId kid = q ? kSingleQuant : kSingle;
-  auto kernel = q ? k_gemm_quant : k_gemm;
-  if (!smem_configured(st, kid, reinterpret_cast<const void*>(kernel))) {
-    *why = "cudaFuncSetAttribute failed";
-    return cudaErrorInvalidValue;
-  }
-  GemmArgs a{A.scales, B.scales, A.g, B.g, (int)A.rows, (int)B.rows, (int)A.K, out_bf16 ? 1 : 0, err,
+  const KernelId kid = q ? kSingleQuant : out_bf16 ? kSingleBf16 : kSingleF32;
+  auto kernel = q ? k_gemm_quant : out_bf16 ? k_gemm<true> : k_gemm<false>;
+  if (!kernel_configured(st, kid, reinterpret_cast<const void*>(kernel), why)) return cudaErrorInvalidValue;
+  GemmArgs a{A.scales, B.scales, A.g, B.g, (int)A.rows, (int)B.rows, (int)A.K, err,
              reinterpret_cast<unsigned int*>(amax_out), q ? *q : GemmQuantOut{}, D, ldd, (int)n_tma, 0u, 0ull};
   if (!q) {
     const unsigned long long lim = take_armed_wait(1);
@@ -1085,23 +1130,21 @@ cudaError_t launch_gemm_grouped(int count, const GemmOperand* A, const GemmOpera
     *why = "device error word unavailable";
     return cudaErrorInvalidValue;
   }
-  if (!smem_configured(st, kGrouped, reinterpret_cast<const void*>(k_gemm_grouped))) {
-    *why = "cudaFuncSetAttribute failed";
-    return cudaErrorInvalidValue;
-  }
+  const KernelId kid = out_bf16 ? kGroupedBf16 : kGroupedF32;
+  auto kernel = out_bf16 ? k_gemm_grouped<true> : k_gemm_grouped<false>;
+  if (!kernel_configured(st, kid, reinterpret_cast<const void*>(kernel), why)) return cudaErrorInvalidValue;
   GroupedArgs g;
   int n = 0, tiles = 0;
   auto flush = [&]() -> cudaError_t {
     if (n == 0) return cudaSuccess;
     g.count = n;
-    g.out_bf16 = out_bf16 ? 1 : 0;
     g.err = err;
     g.tile_start[n] = tiles;
     const int t = tiles;
     n = 0;
     tiles = 0;
     if (t == 0) return cudaSuccess;
-    cudaError_t e = launch_pairs(k_gemm_grouped, t, st, kGrouped, s, g);
+    cudaError_t e = launch_pairs(kernel, t, st, kid, s, g);
     if (e != cudaSuccess) *why = "cudaLaunchKernelEx (cluster of 2) failed";
     return e;
   };

@@ -32,7 +32,6 @@ struct GemmArgs {
   const float* ga;
   const float* gb;
   int M, N, K;
-  int out_bf16;
   unsigned int* err;
   unsigned int* amax_out;  // nullable: atomicMax of |D| (as stored) over the output, float bits
   GemmQuantOut q;          // used by the quantizing variant only
@@ -62,7 +61,6 @@ struct GroupedArgs {
   int M[kGroupsPerLaunch], N[kGroupsPerLaunch], K[kGroupsPerLaunch];
   int tile_start[kGroupsPerLaunch + 1];
   int count;
-  int out_bf16;
   unsigned int* err;
 };
 
