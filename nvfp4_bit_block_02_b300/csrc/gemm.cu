@@ -546,13 +546,13 @@ __device__ __forceinline__ void gemm_pairs(const Sched& sched, unsigned int* err
             const uint32_t sfa = tmem + SFA_COL0 + 16 * s, sfb = tmem + SFB_COL0 + 32 * s;
             const int kc = nkc - 4 * kt;  // K-steps of 64 left: 4 or more except in a K-tail stage
             if (kc >= 4) {
-  #pragma unroll
+#pragma unroll
               for (int j = 0; j < 4; ++j) {
                 tc_mma_pair(tmem, da + 2 * j, db + 2 * j, sfa + 4 * j, sfb + 8 * j, (kt | j) != 0);
                 if (j == 2) next_ready = mbar_test(full0 + 8 * sn, phn);
               }
             } else {
-  #pragma unroll
+#pragma unroll
               for (int j = 0; j < 4; ++j) {
                 if (j < kc) tc_mma_pair(tmem, da + 2 * j, db + 2 * j, sfa + 4 * j, sfb + 8 * j, (kt | j) != 0);
                 if (j == 2) next_ready = mbar_test(full0 + 8 * sn, phn);
@@ -589,7 +589,7 @@ __device__ __forceinline__ void gemm_pairs(const Sched& sched, unsigned int* err
           const uint4* sa = reinterpret_cast<const uint4*>(smem + OFF_SFA + s * SFA_BYTES) + lane;
           const uint4* sb = reinterpret_cast<const uint4*>(smem + OFF_SFB + s * SFB_BYTES) + lane;
           uint32_t va[16], vb[32];
-  #pragma unroll
+#pragma unroll
           for (int j = 0; j < 4; ++j) {
             const uint4 wa = sa[j * 32];
             va[4 * j] = wa.x; va[4 * j + 1] = wa.y; va[4 * j + 2] = wa.z; va[4 * j + 3] = wa.w;
