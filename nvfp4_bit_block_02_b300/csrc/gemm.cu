@@ -585,6 +585,9 @@ __device__ __forceinline__ void gemm_pairs(const Sched& sched, unsigned int* err
             ok = false;
             break;
           }
+          // the slot's previous MMAs completed before these bytes were copied
+          // (the scale producer waited for them): order the stores after them
+          tc_fence_after();
           // lane l: row l of every 512-byte atom = 16 bytes = 4 consecutive columns
           const uint4* sa = reinterpret_cast<const uint4*>(smem + OFF_SFA + s * SFA_BYTES) + lane;
           const uint4* sb = reinterpret_cast<const uint4*>(smem + OFF_SFB + s * SFB_BYTES) + lane;

@@ -18,7 +18,8 @@ def _operands(M, N, K, seed):
     x = torch.from_numpy(synthetic.with_entry_outliers(rng.standard_normal((M, K)).astype(np.float32), 0.01, 30.0,
                                                        seed)).to(torch.bfloat16).cuda()
     w = torch.from_numpy((0.05 * rng.standard_normal((N, K))).astype(np.float32)).to(torch.bfloat16).cuda()
-    return nv.quantize(x), nv.quantize(w, block="2d")
+    # 2D weight blocks need whole 16-row groups; other N take 1D blocks
+    return nv.quantize(x), nv.quantize(w, block="2d" if N % 16 == 0 else "1d")
 
 
 @pytest.mark.parametrize("M,N,K", [(128, 128, 256), (384, 640, 512), (1024, 768, 1024), (256, 384, 2048)])
@@ -47,3 +48,22 @@ def test_gemm_amax_llama8b_full_size():
     nv.sync_check()
     assert torch.equal(d, ref)
     assert float(am.cpu()[0]) == float(d.float().abs().max().cpu())
+
+
+@pytest.mark.parametrize("M,N,K", [(200, 130, 320), (77, 100, 64), (300, 200, 192), (129, 257, 128)])
+@pytest.mark.parametrize("dt", [torch.bfloat16, torch.float32])
+def test_gemm_amax_ragged(M, N, K, dt):
+    """N not a multiple of 128 (an epilogue warp holds fewer than 128 valid
+    columns) nor, for some, of a 16-byte unit (the row's last partial unit
+    goes through plain stores): the amax covers exactly the stored outputs and
+    nothing is written past them."""
+    qa, qb = _operands(M, N, K, 7 * M + N + K)
+    per16 = 16 // (2 if dt == torch.bfloat16 else 4)
+    ld = -(-N // per16) * per16
+    big_ref = torch.full((M + 1, ld + per16), -7.0, dtype=dt, device="cuda")
+    big = big_ref.clone()
+    nv.gemm(qa, qb, out=big_ref[:M, :N])
+    _, am = nv.gemm_amax(qa, qb, out=big[:M, :N])
+    nv.sync_check()
+    assert torch.equal(big, big_ref)  # D identical, padding and the extra row untouched
+    assert float(am.cpu()[0]) == float(big[:M, :N].float().abs().max().cpu())
