@@ -16,8 +16,9 @@ advances the Philox stream.  ``enabled=False`` keeps a layer in BF16 (the
 recipe leaves some layers in higher precision); that path is torch's own
 matmul and does not touch the library.
 
-Shapes: tokens % 256 == 0, out_features % 256 == 0, in_features % 256 == 0
-(each of them is the K of one of the three GEMMs).
+Shapes: tokens, out_features and in_features each a multiple of 64 (each of
+them is the K of one of the three GEMMs, whose K steps by 64); the 2D weight
+blocks and the Hadamard chunks (16) divide that.
 """
 from __future__ import annotations
 
@@ -28,8 +29,8 @@ from . import gemm, quantize, rht_quantize, transpose_2d
 
 def _check_shapes(tokens: int, n_out: int, n_in: int):
     for name, v in (("tokens", tokens), ("out_features", n_out), ("in_features", n_in)):
-        if v % 256:
-            raise ValueError(f"{name} = {v} must be a multiple of 256 (it is the K of one of the layer's GEMMs)")
+        if v % 64:
+            raise ValueError(f"{name} = {v} must be a multiple of 64 (it is the K of one of the layer's GEMMs)")
 
 
 class NVFP4LinearFunction(torch.autograd.Function):

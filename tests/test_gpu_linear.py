@@ -17,7 +17,7 @@ def _oq(t: torch.Tensor, **kw):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("T,n_in,n_out", [(256, 256, 256), (512, 768, 512)])
+@pytest.mark.parametrize("T,n_in,n_out", [(256, 256, 256), (512, 768, 512), (192, 320, 448)])
 def test_linear_forward_backward_matches_oracle(T, n_in, n_out):
     rng = np.random.default_rng(T + n_in + n_out)
     x = torch.from_numpy(synthetic.with_channel_outliers(rng.standard_normal((T, n_in)).astype(np.float32), 0.01,
