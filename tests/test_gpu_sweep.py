@@ -15,7 +15,7 @@ from tests.gpu_helpers import assert_same_quantized, gemm_check, guarded_tensor,
 
 pytestmark = pytest.mark.gpu
 
-N_QUANT, N_GEMM = 48, 24
+N_QUANT, N_GEMM = 160, 96
 
 
 def _quant_case(i):
@@ -86,7 +86,7 @@ def test_gemm_sweep(i):
     gemm_check(full[:M, :N], ref, bound, out_dtype == torch.bfloat16, f"GEMM case {i}: {M}x{N}x{K}")
 
 
-@pytest.mark.parametrize("i", range(16))
+@pytest.mark.parametrize("i", range(48))
 def test_w4a16_sweep(i):
     """Random M, N, K (K % 16 == 0) and a padded output row; the padding keeps
     its canary."""
@@ -106,7 +106,7 @@ def test_w4a16_sweep(i):
     gemm_check(full[:M, :N], y_ref, bound, out_dtype == torch.bfloat16, f"W4A16 case {i}: {M}x{N}x{K}")
 
 
-@pytest.mark.parametrize("i", range(8))
+@pytest.mark.parametrize("i", range(24))
 def test_gemm_grouped_sweep(i):
     """1..6 groups of random shapes (an empty group included at random); each
     group's rows a whole number of 16-byte units, as the grouped call requires."""
@@ -134,7 +134,7 @@ def test_gemm_grouped_sweep(i):
         gemm_check(outs[e].float().cpu().numpy(), ref, bound, out_dtype == torch.bfloat16, f"grouped case {i} group {e}")
 
 
-@pytest.mark.parametrize("i", range(12))
+@pytest.mark.parametrize("i", range(48))
 def test_gemm_quantize_sweep(i):
     """Random M, N (N % 16 == 0), K (K % 64 == 0) and tensor amax (exact,
     loose or saturating): the epilogue encoding equals the oracle's
@@ -160,7 +160,7 @@ def test_gemm_quantize_sweep(i):
     assert_same_quantized(out, ref, f"gemm_quantize case {i}: {M}x{N}x{K}")
 
 
-@pytest.mark.parametrize("i", range(12))
+@pytest.mark.parametrize("i", range(48))
 def test_dequantize_sweep(i):
     """Random shapes, block modes and scalings; the FP32 output bit-exact with
     the oracle's decode, the BF16 output its nearest-even rounding."""
@@ -181,7 +181,7 @@ def test_dequantize_sweep(i):
     assert torch.equal(y16.cpu(), torch.from_numpy(yr).to(torch.bfloat16))
 
 
-@pytest.mark.parametrize("i", range(12))
+@pytest.mark.parametrize("i", range(64))
 def test_rht_sweep(i):
     """Random RHT configurations (orientation, rounding, scaling, dtype, shape,
     value scale, wide-span chunks) under the RHT parity rules of
@@ -201,7 +201,7 @@ def test_rht_sweep(i):
     check_rht(torch.from_numpy(x).to(dtype), transpose, rounding, scaling)
 
 
-@pytest.mark.parametrize("i", range(8))
+@pytest.mark.parametrize("i", range(24))
 def test_quantize_grouped_sweep(i):
     """1..70 tensors of random shapes in one grouped call (a second launch past
     64) with a random mode: every group bit-exact with the single-tensor call
@@ -236,7 +236,7 @@ def test_quantize_grouped_sweep(i):
         assert_same_quantized(qs[e], ref, f"grouped case {i} group {e}")
 
 
-@pytest.mark.parametrize("i", range(8))
+@pytest.mark.parametrize("i", range(48))
 def test_transpose_2d_sweep(i):
     """Random R x K (both % 16) and scaling, RNE: repacking the 2D quantization
     of W equals the oracle's 2D quantization of W^T bit for bit."""
