@@ -78,10 +78,11 @@ def ncu_traffic(kernel: str, src_hash: str, workload: str):
         return None
     with open(p) as f:
         d = json.load(f)
-    e = d.get(kernel)
-    if not e or e.get("source_hash") != src_hash or e.get("bench_workload") != workload:
-        return None
-    return e.get("dram_bytes_per_launch")
+    entries = d.get(kernel) or []
+    for e in entries if isinstance(entries, list) else [entries]:
+        if e.get("source_hash") == src_hash and e.get("bench_workload") == workload:
+            return e.get("dram_bytes_per_launch")
+    return None
 
 
 class ClockSampler:
