@@ -237,6 +237,11 @@ nvfp4_status nvfp4_quantize_grouped(int count, const void* const* x, nvfp4_dtype
     a.scales = o->scales;
     a.seed = cfg->seed;
     a.offset = cfg->offset + (uint64_t)e;
+    a.err = nvfp4::device_error_word();  // bounded waits of the TMA-fed transposed encoder
+    if (!a.err) {
+      st = cuda_fail(cudaGetLastError(), "device error word (cudaGetSymbolAddress)");
+      break;
+    }
     if (n == nvfp4::kQuantGroups) st = flush();
   }
   if (st == NVFP4_OK) st = flush();

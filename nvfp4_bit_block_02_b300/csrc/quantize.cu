@@ -14,8 +14,9 @@
 // 512-byte atom of the scale layout, so every scale byte (padding included)
 // is written by the encoder and no memset is needed.  Loads are 16-byte
 // vectors; the transposed encoder stages a 64 x 128 input tile in shared
-// memory (through a TMA ring for a single tensor) and reads it back as column
-// pairs (32-bit words), conflict-free.
+// memory (through a TMA ring, one tensor map per tensor or group; through
+// registers only when a group's map cannot be built) and reads it back as
+// column pairs (32-bit words), conflict-free.
 #include <atomic>
 
 #include "gemm.h"
@@ -481,7 +482,9 @@ __device__ __forceinline__ void tile_load(void* dst, const CUtensorMap* tm, int 
       : "memory");
 }
 
-// TMA (single tensor, tm != nullptr) or register prefetch (grouped tensors).
+// TMA: input tiles through the ring, from the single tensor's map `tm` or from
+// each tile's group's map in the group arguments; otherwise staged through
+// registers (a group whose map could not be built).
 // hold_tx and wait_ns: the failure-detection test's withheld bytes on each
 // CTA's first tile and its wait limit (both 0 in normal launches: 2 s).
 template <typename T, bool B2D, bool SR, bool F46, bool RHT, bool AMAX_ONLY, bool TMA, class Src>
@@ -536,16 +539,21 @@ __device__ __forceinline__ void quant_cols_body(const Src& src, const QuantArgs&
   [[maybe_unused]] uint32_t k = 0;    // this CTA's tile counter (TMA ring position)
   [[maybe_unused]] uint32_t req = 0;  // (thread 0) tiles requested so far
   [[maybe_unused]] const unsigned long long limit = wait_ns ? wait_ns : 2000000000ull;
+  // the input map of a tile: the single tensor's, or the tile's group's
+  [[maybe_unused]] auto map_of = [&](const typename Src::Ref& r) -> const CUtensorMap* {
+    if constexpr (Src::kGrouped) return &src.g.tm[r.e];
+    else return tm;
+  };
   if constexpr (TMA) {
     if (t == 0) {
-      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map_of(ref))) : "memory");
       abort_s = 0;
 #pragma unroll
       for (int i = 0; i < S; ++i) bar_init(&full[i], 1);
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
       iref = ref;
       for (int i = 0; i < S && have_i; ++i) {
-        tile_load(ring + i * 64 * RB, tm, (int)(iref.tx * 128), (int)(iref.ty * 64), &full[i],
+        tile_load(ring + i * 64 * RB, map_of(iref), (int)(iref.tx * 128), (int)(iref.ty * 64), &full[i],
                   64 * RB + (i == 0 ? hold_tx : 0u));
         ++req;
         typename Src::Ref n;
@@ -595,10 +603,15 @@ __device__ __forceinline__ void quant_cols_body(const Src& src, const QuantArgs&
       if (abort_s) break;  // a tile never landed (uniform after the barrier)
       if (t == 0 && have_i) {
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        tile_load(ring + (k % S) * 64 * RB, tm, (int)(iref.tx * 128), (int)(iref.ty * 64), &full[k % S], 64 * RB);
+        tile_load(ring + (k % S) * 64 * RB, map_of(iref), (int)(iref.tx * 128), (int)(iref.ty * 64), &full[k % S],
+                  64 * RB);
         ++req;
         typename Src::Ref n;
         have_i = src.next(iref, n);
+        if constexpr (Src::kGrouped) {  // the next request's map, when it is another group's
+          if (have_i && n.e != iref.e)
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&src.g.tm[n.e])) : "memory");
+        }
         iref = n;
       }
       ++k;
@@ -699,10 +712,12 @@ __global__ void __launch_bounds__(256) k_quant_cols(const __grid_constant__ CUte
   quant_cols_body<T, B2D, SR, F46, RHT, AMAX_ONLY, true>(src, a, &tm, hold_tx, wait_ns);
 }
 
-template <typename T, bool B2D, bool SR, bool F46>
+// TMA: input tiles through the ring, each group's map in the parameters
+// (else staged through registers).
+template <typename T, bool B2D, bool SR, bool F46, bool TMA>
 __global__ void __launch_bounds__(256) k_quant_cols_grouped(const __grid_constant__ GroupQuant g) {
   const Groups src(g);
-  quant_cols_body<T, B2D, SR, F46, false, false, false>(src, g.a[0]);
+  quant_cols_body<T, B2D, SR, F46, false, false, TMA>(src, g.a[0]);
 }
 
 
@@ -875,8 +890,13 @@ static void launch_qg(const GroupQuant& g, bool transpose, cudaStream_t s) {
     auto k = k_quant_rows_grouped<T, B2D, SR, F46>;
     static OccCache occ = {};
     k<<<persistent_grid(k, tiles, occ), 256, 0, s>>>(g);
+  } else if (g.use_tma) {
+    auto k = k_quant_cols_grouped<T, B2D, SR, F46, true>;
+    constexpr int smem = kColRingBytes<T>;
+    static OccCache occ = {};
+    k<<<persistent_grid(k, tiles, occ, smem), 256, smem, s>>>(g);
   } else {
-    auto k = k_quant_cols_grouped<T, B2D, SR, F46>;
+    auto k = k_quant_cols_grouped<T, B2D, SR, F46, false>;
     static OccCache occ = {};
     k<<<persistent_grid(k, tiles, occ), 256, 0, s>>>(g);
   }
@@ -921,6 +941,14 @@ cudaError_t launch_quantize_grouped(GroupQuant& g, bool bf16, bool transpose, bo
   }
   g.tile_start[g.count] = tiles;
   g.amax_start[g.count] = atiles;
+  g.use_tma = 0;
+  if (transpose) {  // the ring's input maps (64 tokens x 128 columns per tile)
+    g.use_tma = 1;
+    for (int e = 0; e < g.count && g.use_tma; ++e) {
+      const QuantArgs& a = g.a[e];
+      if (!make_tile_map_2d(&g.tm[e], a.x, bf16, a.R_in, a.C_in, a.ld, 128, 64)) g.use_tma = 0;
+    }
+  }
   if (compute_amax) {
     k_zero_group_amax<<<1, kQuantGroups, 0, s>>>(g);
     const unsigned cap = (unsigned)num_sms() * 8;

@@ -1,7 +1,9 @@
 // Internal launch interface of the quantizer kernels (not part of the C ABI).
 #pragma once
-#include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
+
+#include <cstdint>
 
 namespace nvfp4 {
 
@@ -22,15 +24,18 @@ struct QuantArgs {
 };
 
 // Up to kQuantGroups tensors quantized by one amax launch and one encode
-// launch (the MoE experts): per group its own args and tensor amax.
+// launch (the MoE experts): per group its own args and tensor amax, and (the
+// transposed encoder) its input tensor map.
 constexpr int kQuantGroups = 64;
 struct GroupQuant {
+  CUtensorMap tm[kQuantGroups];  // transposed encoder: 64 x 128-element input tiles of each group's x
   QuantArgs a[kQuantGroups];
   uint32_t tiles_x[kQuantGroups];         // encoder tile-grid width per group
   uint32_t tile_start[kQuantGroups + 1];  // encoder tiles, prefix sums
   uint32_t amax_rows[kQuantGroups];       // amax pass: input rows per tile
   uint32_t amax_start[kQuantGroups + 1];  // amax tiles, prefix sums
   int count;
+  int use_tma;  // transposed encoder: every group's map was built (else register staging)
 };
 
 // Fills the tile tables of g (count and a[] set by the caller), then
