@@ -734,6 +734,14 @@ __global__ void __launch_bounds__(256) k_quant_cols_grouped(const __grid_constan
   const Groups src(g);
   quant_cols_body<T, B2D, SR, F46, false, false, TMA>(src, g.a[0]);
 }
+// The TMA-fed encode without stochastic rounding fits 80 registers: 3 CTAs per
+// SM (192 KB of rings) hide more of its ALU latency (MoE Four-over-Six
+// weights 578 -> 561 us; with SR it spills and stays at 2).
+template <typename T, bool B2D, bool F46>
+__global__ void __launch_bounds__(256, 3) k_quant_cols_grouped3(const __grid_constant__ GroupQuant g) {
+  const Groups src(g);
+  quant_cols_body<T, B2D, false, F46, false, false, true>(src, g.a[0]);
+}
 
 
 // ---------------------------------------------------------------------------
@@ -918,10 +926,16 @@ static void launch_qg(const GroupQuant& g, bool transpose, cudaStream_t s) {
       k<<<persistent_grid(k, tiles, occ), 256, 0, s>>>(g);
     }
   } else if (g.use_tma) {
-    auto k = k_quant_cols_grouped<T, B2D, SR, F46, true>;
     constexpr int smem = kColRingBytes<T>;
-    static OccCache occ = {};
-    k<<<persistent_grid(k, tiles, occ, smem), 256, smem, s>>>(g);
+    if constexpr (!SR) {
+      auto k = k_quant_cols_grouped3<T, B2D, F46>;
+      static OccCache occ = {};
+      k<<<persistent_grid(k, tiles, occ, smem), 256, smem, s>>>(g);
+    } else {
+      auto k = k_quant_cols_grouped<T, B2D, SR, F46, true>;
+      static OccCache occ = {};
+      k<<<persistent_grid(k, tiles, occ, smem), 256, smem, s>>>(g);
+    }
   } else {
     auto k = k_quant_cols_grouped<T, B2D, SR, F46, false>;
     static OccCache occ = {};
