@@ -10,16 +10,19 @@
 // weight instead of 2 for BF16).
 //
 // Layout of the work: a CTA of 4 warps owns 16 weight rows; warp w takes the
-// 64-wide K tiles w, w + 4, ...; the 4 partial results meet in shared memory.
+// K tiles w, w + 4, ...; the 4 partial results meet in shared memory.
 // The products run on register-operand BF16 MMAs (m16n8k16, FP32
 // accumulate): weight rows are the MMA's M, tokens its N (8 per MMA), the
 // decoded BF16 pairs are the A fragment directly and the activations' BF16
 // pairs the B fragment directly, so nothing is unpacked per token.  The sum
-// over K does not depend on the order of its terms, so inside each 64-wide
-// tile the K positions are permuted to suit the decode: lane (g, t) decodes
-// the whole 16-element block t of rows g and g + 8 (8 code bytes and one
-// scale each) and feeds the four MMAs of the tile with its own pairs; its B
-// fragments are the activations at the same K positions (one 32-byte run).
+// over K does not depend on the order of its terms, so inside each K tile
+// the K positions are permuted to suit the decode: lane (g, t) decodes
+// whole 16-element blocks of rows g and g + 8 and feeds four MMAs per block
+// with its own pairs; its B fragments are the activations at the same K
+// positions (one 32-byte run per block).  With K % 32 == 0 a K tile is 128
+// wide and lane t takes blocks 2t and 2t + 1 of it (16 code bytes and two
+// adjacent scale bytes per row in one load each); otherwise a tile is 64
+// wide and lane t takes block t (8 code bytes, one scale).
 #include "nvfp4_device.cuh"
 #include "quantize.h"
 
@@ -55,18 +58,53 @@ __device__ __forceinline__ uint2 ld_stream_u2(const uint8_t* p) {
   asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
   return r;
 }
+__device__ __forceinline__ uint4 ld_stream_u4(const uint8_t* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+// The codes (8 BPL bytes) and scales (BPL bytes) of a lane's BPL blocks of
+// one row; block h's codes are words 2h, 2h + 1 and its scale byte h.
+template <int BPL>
+struct W4Blocks {
+  uint32_t c[2 * BPL];
+  uint32_t s;
+  __device__ __forceinline__ void clear() {
+#pragma unroll
+    for (int i = 0; i < 2 * BPL; ++i) c[i] = 0u;
+    s = 0u;
+  }
+  __device__ __forceinline__ void load(const uint8_t* codes, const uint8_t* scales) {
+    if constexpr (BPL == 2) {
+      const uint4 v = ld_stream_u4(codes);
+      c[0] = v.x, c[1] = v.y, c[2] = v.z, c[3] = v.w;
+      s = *reinterpret_cast<const uint16_t*>(scales);
+    } else {
+      const uint2 v = ld_stream_u2(codes);
+      c[0] = v.x, c[1] = v.y;
+      s = *scales;
+    }
+  }
+};
 
 constexpr int kW4Warps = 4;   // warps per CTA, splitting K
-constexpr int kW4Unroll = 2;  // K tiles per warp whose loads are issued together
+// K tiles per warp whose loads are issued together: two 64-wide tiles, or one
+// 128-wide tile (the same bytes per lane)
+template <int BPL>
+constexpr int kW4Unroll = BPL == 2 ? 1 : 2;
 constexpr int kW4AccMax = 2;  // independent accumulators per token tile (MMA j of a tile -> j % kW4Acc)
 
-// NT = token tiles of 8 per pass over the weights (tokens m0 .. m0 + 8 NT - 1).
-template <int NT, bool OUT_BF16>
-__global__ void __launch_bounds__(kW4Warps * 32, 8) k_w4a16(const __nv_bfloat16* __restrict__ x, int64_t M,
-                                                           int64_t ldx, const uint8_t* __restrict__ codes,
-                                                           const uint8_t* __restrict__ scales,
-                                                           const float* __restrict__ gptr, int64_t N, int64_t K,
-                                                           void* __restrict__ y, int64_t ldy) {
+// NT = token tiles of 8 per pass over the weights (tokens m0 .. m0 + 8 NT - 1);
+// BPL = blocks per lane and row in a K tile (the tile is 64 BPL wide).
+// The 128-wide tiles hold more registers: 7 CTAs per SM (72 registers).
+template <int NT, bool OUT_BF16, int BPL>
+__global__ void __launch_bounds__(kW4Warps * 32, BPL == 1 ? 8 : 7)
+    k_w4a16(const __nv_bfloat16* __restrict__ x, int64_t M, int64_t ldx, const uint8_t* __restrict__ codes,
+            const uint8_t* __restrict__ scales, const float* __restrict__ gptr, int64_t N, int64_t K,
+            void* __restrict__ y, int64_t ldy) {
   // two token tiles already give each warp two independent MMA chains (and one accumulator each avoids spills)
   constexpr int kW4Acc = NT == 1 ? kW4AccMax : 1;
   __shared__ float part[kW4Warps][NT][8][17];
@@ -76,14 +114,17 @@ __global__ void __launch_bounds__(kW4Warps * 32, 8) k_w4a16(const __nv_bfloat16*
   const bool va = ra < N, vb = ra + 8 < N;
   const float gs = *gptr;
   const float2 g2 = make_float2(gs, gs);
-  const int KB = (int)(K / 16), KT = (KB + 3) / 4;
-  // block (row, kt * 4 + t) has its codes at row * K/2 + kt * 32 + 8t and its
-  // scale at sf_offset(row, kt * 4 + t) = sf_offset(row, t) + kt * 512; row
-  // ra + 8 lies in the same 32-row group as ra (16-row aligned n0, g < 8), so
-  // its scales sit 128 bytes on and its codes 8 rows (4K bytes) on
+  const int KB = (int)(K / 16), KT = (KB + 4 * BPL - 1) / (4 * BPL), nka = (KB + 3) / 4;
+  // block (row, kt * 4 BPL + BPL t + h) has its codes at row * K/2 +
+  // kt * 32 BPL + 8 (BPL t + h) and its scale at sf_offset(row, BPL t + h) +
+  // kt * 512 BPL (the BPL scales of a lane are adjacent bytes of one 128x4
+  // atom); row ra + 8 lies in the same 32-row group as ra (16-row aligned
+  // n0, g < 8), so its scales sit 128 bytes on and its codes 8 rows (4K
+  // bytes) on.  With BPL = 2, K % 32 == 0: a lane's second block is valid
+  // whenever its first is.
   const int64_t row8 = 4 * K;
-  const uint8_t* pa = codes + ra * (K / 2) + 8 * t;
-  const uint8_t* qa = scales + sf_offset(ra, t, KT);
+  const uint8_t* pa = codes + ra * (K / 2) + 8 * BPL * t;
+  const uint8_t* qa = scales + sf_offset(ra, BPL * t, nka);
   for (int64_t m0 = 0; m0 < M; m0 += 8 * NT) {
     float accj[NT][kW4Acc][4];
 #pragma unroll
@@ -96,46 +137,42 @@ __global__ void __launch_bounds__(kW4Warps * 32, 8) k_w4a16(const __nv_bfloat16*
     for (int i = 0; i < NT; ++i) {
       const int64_t tok = m0 + 8 * i + g;
       xv[i] = tok < M;
-      xr[i] = x + (xv[i] ? tok : 0) * ldx + 16 * t;
+      xr[i] = x + (xv[i] ? tok : 0) * ldx + 16 * BPL * t;
     }
-    for (int kt0 = warp; kt0 < KT; kt0 += kW4Warps * kW4Unroll) {
-      uint2 ca[kW4Unroll], cb[kW4Unroll];
-      uint32_t sa[kW4Unroll], sb[kW4Unroll];
+    for (int kt0 = warp; kt0 < KT; kt0 += kW4Warps * kW4Unroll<BPL>) {
+      W4Blocks<BPL> wa_in[kW4Unroll<BPL>], wb_in[kW4Unroll<BPL>];
 #pragma unroll
-      for (int u = 0; u < kW4Unroll; ++u) {
+      for (int u = 0; u < kW4Unroll<BPL>; ++u) {
         const int kt = kt0 + kW4Warps * u;
-        const bool ok = kt < KT && kt * 4 + t < KB;
-        ca[u] = cb[u] = make_uint2(0u, 0u);
-        sa[u] = sb[u] = 0u;
-        if (ok && va) {
-          ca[u] = ld_stream_u2(pa + (uint32_t)kt * 32u);
-          sa[u] = qa[(uint32_t)kt * 512u];
-        }
-        if (ok && vb) {
-          cb[u] = ld_stream_u2(pa + row8 + (uint32_t)kt * 32u);
-          sb[u] = qa[128u + (uint32_t)kt * 512u];
-        }
+        const bool ok = kt < KT && kt * 4 * BPL + BPL * t < KB;
+        wa_in[u].clear();
+        wb_in[u].clear();
+        if (ok && va) wa_in[u].load(pa + (uint32_t)kt * (32u * BPL), qa + (uint32_t)kt * (512u * BPL));
+        if (ok && vb) wb_in[u].load(pa + row8 + (uint32_t)kt * (32u * BPL), qa + 128u + (uint32_t)kt * (512u * BPL));
       }
 #pragma unroll
-      for (int u = 0; u < kW4Unroll; ++u) {
+      for (int u = 0; u < kW4Unroll<BPL>; ++u) {
         const int kt = kt0 + kW4Warps * u;
         if (kt < KT) {  // warp-uniform
-          const bool ok = kt * 4 + t < KB;
-          uint32_t wa[8], wb[8];
-          w4a16_block(ca[u], sa[u], g2, wa);
-          w4a16_block(cb[u], sb[u], g2, wb);
+          const bool ok = kt * 4 * BPL + BPL * t < KB;
 #pragma unroll
-          for (int i = 0; i < NT; ++i) {
-            uint4 xa = make_uint4(0u, 0u, 0u, 0u), xb = xa;
-            if (xv[i] && ok) {
-              const uint4* p = reinterpret_cast<const uint4*>(xr[i] + (uint32_t)kt * 64u);
-              xa = __ldg(p);
-              xb = __ldg(p + 1);
+          for (int h = 0; h < BPL; ++h) {
+            uint32_t wa[8], wb[8];
+            w4a16_block(make_uint2(wa_in[u].c[2 * h], wa_in[u].c[2 * h + 1]), wa_in[u].s >> (8 * h), g2, wa);
+            w4a16_block(make_uint2(wb_in[u].c[2 * h], wb_in[u].c[2 * h + 1]), wb_in[u].s >> (8 * h), g2, wb);
+#pragma unroll
+            for (int i = 0; i < NT; ++i) {
+              uint4 xa = make_uint4(0u, 0u, 0u, 0u), xb = xa;
+              if (xv[i] && ok) {
+                const uint4* p = reinterpret_cast<const uint4*>(xr[i] + (uint32_t)kt * (64u * BPL) + 16 * h);
+                xa = __ldg(p);
+                xb = __ldg(p + 1);
+              }
+              mma_bf16_16816(accj[i][0 % kW4Acc], wa[0], wb[0], wa[1], wb[1], xa.x, xa.y);
+              mma_bf16_16816(accj[i][1 % kW4Acc], wa[2], wb[2], wa[3], wb[3], xa.z, xa.w);
+              mma_bf16_16816(accj[i][2 % kW4Acc], wa[4], wb[4], wa[5], wb[5], xb.x, xb.y);
+              mma_bf16_16816(accj[i][3 % kW4Acc], wa[6], wb[6], wa[7], wb[7], xb.z, xb.w);
             }
-            mma_bf16_16816(accj[i][0 % kW4Acc], wa[0], wb[0], wa[1], wb[1], xa.x, xa.y);
-            mma_bf16_16816(accj[i][1 % kW4Acc], wa[2], wb[2], wa[3], wb[3], xa.z, xa.w);
-            mma_bf16_16816(accj[i][2 % kW4Acc], wa[4], wb[4], wa[5], wb[5], xb.x, xb.y);
-            mma_bf16_16816(accj[i][3 % kW4Acc], wa[6], wb[6], wa[7], wb[7], xb.z, xb.w);
           }
         }
       }
@@ -179,13 +216,20 @@ cudaError_t launch_w4a16(const void* x, int64_t M, int64_t ldx, const uint8_t* c
   const unsigned grid = (unsigned)((N + 15) / 16);
   const __nv_bfloat16* xp = reinterpret_cast<const __nv_bfloat16*>(x);
   const dim3 block(kW4Warps * 32);
-  if (M <= 8) {
-    if (out_bf16) k_w4a16<1, true><<<grid, block, 0, s>>>(xp, M, ldx, codes, scales, g, N, K, y, ldy);
-    else k_w4a16<1, false><<<grid, block, 0, s>>>(xp, M, ldx, codes, scales, g, N, K, y, ldy);
+  // 16-byte code loads need K % 32 == 0 (rows of 16-byte multiples); with
+  // two token tiles the wide form would spill, so it serves M <= 8
+#define NVFP4_W4_LAUNCH(NT, BF, BPL) k_w4a16<NT, BF, BPL><<<grid, block, 0, s>>>(xp, M, ldx, codes, scales, g, N, K, y, ldy)
+  if (M <= 8 && K % 32 == 0) {
+    if (out_bf16) NVFP4_W4_LAUNCH(1, true, 2);
+    else NVFP4_W4_LAUNCH(1, false, 2);
+  } else if (M <= 8) {
+    if (out_bf16) NVFP4_W4_LAUNCH(1, true, 1);
+    else NVFP4_W4_LAUNCH(1, false, 1);
   } else {
-    if (out_bf16) k_w4a16<2, true><<<grid, block, 0, s>>>(xp, M, ldx, codes, scales, g, N, K, y, ldy);
-    else k_w4a16<2, false><<<grid, block, 0, s>>>(xp, M, ldx, codes, scales, g, N, K, y, ldy);
+    if (out_bf16) NVFP4_W4_LAUNCH(2, true, 1);
+    else NVFP4_W4_LAUNCH(2, false, 1);
   }
+#undef NVFP4_W4_LAUNCH
   return cudaGetLastError();
 }
 

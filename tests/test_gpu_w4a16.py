@@ -76,6 +76,19 @@ def test_w4a16_identity_activations_reproduce_the_bf16_decode():
     np.testing.assert_array_equal(y, w_hat.T)
 
 
+@pytest.mark.parametrize("K", [96, 80, 256])
+def test_w4a16_unit_rows_reproduce_the_bf16_decode_at_small_m(K):
+    """x = 8 rows of I at a time (the single-token-tile launches, K % 32 == 0
+    or not): y[m][n] = W_hat[n][m0 + m] bit for bit, every K position once."""
+    N = 72
+    q, ref = random_weight(N, K, 13 + K)
+    w_hat = oracle.bf16_round(oracle.dequantize(ref.codes, ref.scales, ref.g))
+    eye = torch.eye(K, dtype=torch.bfloat16)
+    for m0 in range(0, K, 8):
+        y, _ = run(eye[m0:m0 + 8].contiguous(), q, torch.float32)
+        np.testing.assert_array_equal(y, w_hat[:, m0:m0 + 8].T, err_msg=f"K={K} rows {m0}..{m0 + 7}")
+
+
 def test_w4a16_closed_form_all_ones():
     """Codes 0x22 (value 1), scales 0x38 (1.0), g = 1, x = 1: y = K exactly."""
     N, K = 96, 2048
