@@ -175,7 +175,8 @@ nvfp4_status nvfp4_rht_quantize(const void* x, nvfp4_dtype xt, int64_t rows, int
  * nvfp4_dequantize - y = fl(fl(value(code) * s_b) * g), BF16 output rounded
  * from that fp32 value (nearest even).
  *   q  host struct with device buffers (codes, scales, global_scale read).
- *   y  device, row-major [q->rows][q->cols] of dtype yt, 16-byte aligned.
+ *   y  device, row-major [q->rows][q->cols] of dtype yt, 16-byte aligned
+ *      (32-byte aligned, each block's output leaves in one 256-bit store).
  */
 nvfp4_status nvfp4_dequantize(const nvfp4_tensor* q, void* y, nvfp4_dtype yt, void* stream);
 

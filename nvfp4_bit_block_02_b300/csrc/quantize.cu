@@ -745,9 +745,17 @@ __global__ void __launch_bounds__(256, 3) k_quant_cols_grouped3(const __grid_con
 
 
 // ---------------------------------------------------------------------------
-// Decoder: one thread per block of 16 (grid-stride).
+// Decoder: one thread per block of 16 (grid-stride), the next block's codes
+// and scale requested before the current one is decoded.  V8: the output is
+// 32-byte aligned and each 32 bytes leave in one 256-bit store.
 // ---------------------------------------------------------------------------
-template <typename TO>
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t w[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+               "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
+template <typename TO, bool V8>
 __global__ void __launch_bounds__(256) k_dequant(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales,
                                                  const float* __restrict__ gptr, int64_t R, int64_t K, TO* __restrict__ y) {
   const float g = *gptr;
@@ -763,18 +771,45 @@ __global__ void __launch_bounds__(256) k_dequant(const uint8_t* __restrict__ cod
   uint32_t kb = (uint32_t)(b0 % KB);
   const uint64_t step_r = step / KB;
   const uint32_t step_kb = (uint32_t)(step % KB);
+  uint2 c = __ldg(reinterpret_cast<const uint2*>(codes + r * (uint64_t)(K / 2) + kb * 8u));
+  uint32_t sb = __ldg(scales + sf_offset((int64_t)r, kb, nka));
   for (uint64_t b = b0; b < nblk; b += step) {
-    const uint2 c = *reinterpret_cast<const uint2*>(codes + r * (uint64_t)(K / 2) + kb * 8u);
-    const uint32_t s2 = e4m3_f16x2_splat(scales[sf_offset((int64_t)r, kb, nka)] & 0x7Fu);
+    uint64_t nr = r + step_r;
+    uint32_t nkb = kb + step_kb;
+    if (nkb >= KB) {
+      nkb -= KB;
+      ++nr;
+    }
+    uint2 cn = make_uint2(0u, 0u);
+    uint32_t sn = 0u;
+    if (b + step < nblk) {
+      cn = __ldg(reinterpret_cast<const uint2*>(codes + nr * (uint64_t)(K / 2) + nkb * 8u));
+      sn = __ldg(scales + sf_offset((int64_t)nr, nkb, nka));
+    }
+    const uint32_t s2 = e4m3_f16x2_splat(sb & 0x7Fu);
     uint32_t h[8];
     e2m1x16_f16x2(c, h);
     float2 o[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) o[i] = decode_pair(h[i], s2, g2);
+    TO* dst = y + r * (uint64_t)K + kb * 16u;
     if constexpr (sizeof(TO) == 4) {
-      float4* d = reinterpret_cast<float4*>(y + r * (uint64_t)K + kb * 16u);
+      if constexpr (V8) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) d[i] = make_float4(o[2 * i].x, o[2 * i].y, o[2 * i + 1].x, o[2 * i + 1].y);
+        for (int q = 0; q < 2; ++q) {
+          uint32_t w[8];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            w[2 * i] = __float_as_uint(o[4 * q + i].x);
+            w[2 * i + 1] = __float_as_uint(o[4 * q + i].y);
+          }
+          st_global_v8(dst + 8 * q, w);
+        }
+      } else {
+        float4* d = reinterpret_cast<float4*>(dst);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) d[i] = make_float4(o[2 * i].x, o[2 * i].y, o[2 * i + 1].x, o[2 * i + 1].y);
+      }
     } else {
       uint32_t w[8];
 #pragma unroll
@@ -782,16 +817,18 @@ __global__ void __launch_bounds__(256) k_dequant(const uint8_t* __restrict__ cod
         __nv_bfloat162 p = __floats2bfloat162_rn(o[i].x, o[i].y);
         w[i] = *reinterpret_cast<uint32_t*>(&p);
       }
-      uint4* d = reinterpret_cast<uint4*>(y + r * (uint64_t)K + kb * 16u);
-      d[0] = make_uint4(w[0], w[1], w[2], w[3]);
-      d[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      if constexpr (V8) {
+        st_global_v8(dst, w);
+      } else {
+        uint4* d = reinterpret_cast<uint4*>(dst);
+        d[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        d[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      }
     }
-    kb += step_kb;
-    r += step_r;
-    if (kb >= KB) {
-      kb -= KB;
-      ++r;
-    }
+    c = cn;
+    sb = sn;
+    r = nr;
+    kb = nkb;
   }
 }
 
@@ -1030,10 +1067,16 @@ cudaError_t launch_dequantize(const uint8_t* codes, const uint8_t* scales, const
   if (nblk == 0) return cudaSuccess;
   int64_t want = (nblk + 255) / 256, cap = (int64_t)num_sms() * 16;
   unsigned grid = (unsigned)(want > cap ? cap : want);
-  if (bf16_out)
-    k_dequant<__nv_bfloat16><<<grid, 256, 0, s>>>(codes, scales, g, R, K, reinterpret_cast<__nv_bfloat16*>(y));
-  else
-    k_dequant<float><<<grid, 256, 0, s>>>(codes, scales, g, R, K, reinterpret_cast<float*>(y));
+  const bool v8 = reinterpret_cast<uintptr_t>(y) % 32 == 0;  // rows are 32-byte multiples (K % 16 == 0)
+  if (bf16_out) {
+    __nv_bfloat16* yb = reinterpret_cast<__nv_bfloat16*>(y);
+    if (v8) k_dequant<__nv_bfloat16, true><<<grid, 256, 0, s>>>(codes, scales, g, R, K, yb);
+    else k_dequant<__nv_bfloat16, false><<<grid, 256, 0, s>>>(codes, scales, g, R, K, yb);
+  } else {
+    float* yf = reinterpret_cast<float*>(y);
+    if (v8) k_dequant<float, true><<<grid, 256, 0, s>>>(codes, scales, g, R, K, yf);
+    else k_dequant<float, false><<<grid, 256, 0, s>>>(codes, scales, g, R, K, yf);
+  }
   return cudaGetLastError();
 }
 

@@ -80,3 +80,28 @@ def test_dequantize_grid_stride_wraps_rows():
     ref = oracle_quantize_like(x.float())
     yr = oracle.dequantize(ref.codes, ref.scales, ref.g)
     assert (y32.cpu().numpy().view(np.uint32) == yr.view(np.uint32)).all()
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_dequantize_output_aligned_to_16_bytes_only(dtype):
+    """An output that starts 16 bytes past a 32-byte boundary (the decoder's
+    256-bit stores need 32): the 16-byte store path, bit-exact, and the bytes
+    around the output untouched."""
+    rows, cols = 96, 208
+    x = torch.from_numpy(synthetic.normal((rows, cols), 1.0, 53))
+    q = nv.quantize(x.cuda())
+    es = 4 if dtype == torch.float32 else 2
+    lead = 16 // es
+    buf = torch.full((rows * cols + 2 * lead,), -3.0, dtype=dtype, device="cuda")
+    y = buf[lead:lead + rows * cols].view(rows, cols)
+    assert y.data_ptr() % 32 == 16
+    nv.dequantize(q, dtype, out=y)
+    nv.sync_check()
+    ref = oracle_quantize_like(x)
+    yr = oracle.dequantize(ref.codes, ref.scales, ref.g)
+    if dtype == torch.float32:
+        assert (y.cpu().numpy().view(np.uint32) == yr.view(np.uint32)).all()
+    else:
+        assert torch.equal(y.cpu(), torch.from_numpy(yr).to(torch.bfloat16))
+    edges = torch.cat([buf[:lead], buf[lead + rows * cols:]]).float().cpu()
+    assert (edges == -3.0).all()
