@@ -61,7 +61,8 @@ __global__ void __launch_bounds__(256) k_amax(const T* __restrict__ x, int64_t r
   for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
     const uint4* row = base + r * ld_vec;
     int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    // 8 loads in flight per thread (128 B), then their maxima
+    // 8 loads in flight per thread (128 B), then their maxima; the last
+    // (partial) batch issues its loads together as well
     for (; v + 7 * stride < nvec; v += 8 * stride) {
       uint4 q[8];
 #pragma unroll
@@ -69,7 +70,13 @@ __global__ void __launch_bounds__(256) k_amax(const T* __restrict__ x, int64_t r
 #pragma unroll
       for (int i = 0; i < 8; ++i) m = max(m, absmax_bits(q[i], T()));
     }
-    for (; v < nvec; v += stride) m = max(m, absmax_bits(__ldg(row + v), T()));
+    if (v < nvec) {
+      uint4 q[7];
+#pragma unroll
+      for (int i = 0; i < 7; ++i) q[i] = v + i * stride < nvec ? __ldg(row + v + i * stride) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int i = 0; i < 7; ++i) m = max(m, absmax_bits(q[i], T()));
+    }
   }
   cta_max_to_global(m, out);
 }
@@ -104,8 +111,24 @@ __global__ void __launch_bounds__(256) k_amax_grouped(const __grid_constant__ Gr
     const int64_t r1 = min(r0 + (int64_t)g.amax_rows[e], a.R_in);
     const uint4* base = reinterpret_cast<const uint4*>(a.x);
     uint32_t m = 0;
-    for (int64_t r = r0; r < r1; ++r)
-      for (int64_t v = threadIdx.x; v < nvec; v += blockDim.x) m = max(m, absmax_bits(__ldg(base + r * ldv + v), T()));
+    if (ldv == nvec) {
+      // contiguous rows: the tile is one run of vectors, 8 loads per thread in flight
+      const uint4* run = base + r0 * nvec;
+      const int64_t n = (r1 - r0) * nvec;
+      for (int64_t v = threadIdx.x; v < n; v += 8 * (int64_t)blockDim.x) {
+        uint4 q[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int64_t j = v + i * (int64_t)blockDim.x;
+          q[i] = j < n ? __ldg(run + j) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) m = max(m, absmax_bits(q[i], T()));
+      }
+    } else {
+      for (int64_t r = r0; r < r1; ++r)
+        for (int64_t v = threadIdx.x; v < nvec; v += blockDim.x) m = max(m, absmax_bits(__ldg(base + r * ldv + v), T()));
+    }
     cta_max_atomic(m, reinterpret_cast<unsigned int*>(a.amax_accum));
   }
 }
