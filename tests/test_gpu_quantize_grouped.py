@@ -52,6 +52,32 @@ def test_grouped_equals_single_calls(count, mode, dtype):
         assert_same_quantized(qs[e], ref, f"group {e} vs oracle")
 
 
+@pytest.mark.parametrize("mode", ["1d", "t_46"])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_grouped_row_strided_inputs(mode, dtype):
+    """Groups given as column slices of wider buffers (row stride > cols): the
+    amax pass walks such tiles row by row; every group bit-exact with the
+    single call on the same view and, for two groups, with the oracle."""
+    rng = np.random.default_rng(77 + len(mode))
+    transpose = mode.startswith("t_")
+    kw = dict(transpose=transpose, scaling="four_over_six" if "46" in mode else "max6", seed=3, offset=7)
+    views = []
+    for x in _tensors(9, rng, dtype, transpose, False):
+        r, c = x.shape
+        wide = torch.full((r, c + 64), 1e4, dtype=dtype)  # the columns past c must be ignored
+        wide[:, :c] = x
+        views.append(wide.cuda()[:, :c])
+    assert all(v.stride(0) == v.shape[1] + 64 for v in views)
+    qs = nv.quantize_grouped(views, **kw)
+    nv.sync_check()
+    for e, v in enumerate(views):
+        _same(qs[e], nv.quantize(v, **{**kw, "offset": kw["offset"] + e}), f"group {e}")
+    for e in (0, len(views) - 1):
+        ref = oracle_quantize_like(views[e].cpu().contiguous(), transpose=transpose,
+                                   four_over_six="46" in mode, seed=3, offset=7 + e)
+        assert_same_quantized(qs[e], ref, f"group {e} vs oracle")
+
+
 def test_grouped_with_empty_groups():
     xs = [torch.randn(64, 64, device="cuda"), torch.zeros((0, 64), device="cuda"), torch.randn(32, 128, device="cuda")]
     qs = nv.quantize_grouped(xs)
